@@ -1,0 +1,221 @@
+// api.cu -- the extern "C" entry points of libq8attn.so (declared in
+// include/q8attn.h): host-side argument validation, the Q tensor map, and the
+// launches.  Every argument is checked before the first CUDA call, so argument
+// errors never touch the device.
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/q8attn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+int ok() {
+  g_err[0] = '\0';
+  return Q8A_OK;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(Q8A_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int32_t> g_inject{0};
+
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link to libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int check_common(int64_t batch, int32_t heads, int32_t head_dim, const char* fn) {
+  if (batch < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: batch must be >= 0 (got %lld)", fn, (long long)batch);
+  if (heads <= 0) return fail(Q8A_ERR_INVALID_ARG, "%s: heads must be > 0 (got %d)", fn, heads);
+  if (head_dim != 64) return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 (got %d)", fn, head_dim);
+  return Q8A_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t q8a_abi_version(void) { return Q8A_ABI_VERSION; }
+
+const char* q8a_last_error(void) { return g_err; }
+
+int64_t q8a_plane_stride_bytes(int64_t n_tokens) {
+  if (n_tokens < 0) return -1;
+  return (n_tokens * Q8A_ROW_BYTES + 15) / 16 * 16;
+}
+
+int q8kv_quantize(const float* x, void* q8_out, int64_t batch, int64_t n_tokens, int32_t heads,
+                  int32_t head_dim, int64_t out_plane_stride_bytes, void* stream) {
+  const char* fn = "q8kv_quantize";
+  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (n_tokens < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_tokens must be >= 0", fn);
+  if (batch == 0 || n_tokens == 0) return ok();
+  if (!x || !q8_out) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (out_plane_stride_bytes < n_tokens * Q8A_ROW_BYTES)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < n_tokens*68 = %lld", fn,
+                (long long)out_plane_stride_bytes, (long long)(n_tokens * Q8A_ROW_BYTES));
+  if (!aligned(x, 16) || !aligned(q8_out, 16) || out_plane_stride_bytes % 16)
+    return fail(Q8A_ERR_MISALIGNED, "%s: x, q8_out and the plane stride must be 16-byte aligned", fn);
+  cudaError_t e = q8a::launch_quantize(x, static_cast<uint8_t*>(q8_out), batch, n_tokens, heads,
+                                       out_plane_stride_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+int attn_state_init(float* m, float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
+                    int32_t head_dim, void* stream) {
+  const char* fn = "attn_state_init";
+  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (n_q < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q must be >= 0", fn);
+  if (batch == 0 || n_q == 0) return ok();
+  if (!m || !l || !o) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned(m, 4) || !aligned(l, 4) || !aligned(o, 16))
+    return fail(Q8A_ERR_MISALIGNED, "%s: m, l need 4-byte and o 16-byte alignment", fn);
+  cudaError_t e = q8a::launch_state_init(m, l, o, batch * heads * n_q, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                    int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
+                    float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
+                    float scale, int32_t causal, void* stream) {
+  const char* fn = "attn_chunk_step";
+  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (n_q < 0 || kv_len < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q and kv_len must be >= 0", fn);
+  if (q_pos0 < 0 || kv_start < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: positions must be >= 0", fn);
+  if (!(scale > 0.0f) || !std::isfinite(scale))
+    return fail(Q8A_ERR_INVALID_ARG, "%s: scale must be finite and > 0", fn);
+  if (batch == 0 || n_q == 0 || kv_len == 0) return ok();
+  if (!q || !k_q8 || !v_q8 || !m || !l || !o) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (kv_plane_stride_bytes < kv_len * Q8A_ROW_BYTES)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < kv_len*68 = %lld", fn,
+                (long long)kv_plane_stride_bytes, (long long)(kv_len * Q8A_ROW_BYTES));
+  if (!aligned(q, 16) || !aligned(k_q8, 16) || !aligned(v_q8, 16) || kv_plane_stride_bytes % 16 ||
+      !aligned(o, 16) || !aligned(m, 4) || !aligned(l, 4))
+    return fail(Q8A_ERR_MISALIGNED,
+                "%s: q, k_q8, v_q8, o and the plane stride need 16-byte alignment; m, l 4-byte", fn);
+  if (kv_len > 0x7FFFFFFFll || n_q > 0x7FFFFFFFll || (int64_t)heads * 64 * 2 * n_q >= (1ll << 40))
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: sizes beyond the supported range", fn);
+
+  // Query tiles that can see any key of this chunk.
+  int64_t first_row = 0;
+  if (causal) {
+    first_row = kv_start - q_pos0;
+    if (first_row >= n_q) return ok();   // every query precedes the chunk
+    if (first_row < 0) first_row = 0;
+  }
+  const int64_t tile0 = first_row / 128;
+  const int64_t n_qtiles = (n_q + 127) / 128 - tile0;
+  if (n_qtiles * batch * heads > 0x7FFFFFFFll)
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: too many query tiles for one launch", fn);
+
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
+  CUtensorMap qmap;
+  std::memset(&qmap, 0, sizeof(qmap));
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(heads) * 64, static_cast<cuuint64_t>(n_q),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * 64 * 2,
+                                 static_cast<cuuint64_t>(heads) * 64 * 2 * static_cast<cuuint64_t>(n_q)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult cr = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", fn, (int)cr);
+
+  q8a::ChunkArgs a{};
+  a.k8 = static_cast<const uint8_t*>(k_q8);
+  a.v8 = static_cast<const uint8_t*>(v_q8);
+  a.m = m;
+  a.l = l;
+  a.o = o;
+  a.plane_stride = kv_plane_stride_bytes;
+  a.q_pos0 = q_pos0;
+  a.kv_start = kv_start;
+  a.kv_len = kv_len;
+  a.n_q = n_q;
+  a.heads = heads;
+  a.bh = static_cast<int32_t>(batch * heads);
+  a.tile0 = static_cast<int32_t>(tile0);
+  a.n_qtiles = static_cast<int32_t>(n_qtiles);
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal ? 1 : 0;
+  a.inject = g_inject.exchange(0);
+  a.timeout_ns = g_timeout_ns.load();
+  cudaError_t e = q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+int attn_finalize(const float* l, const float* o, void* out, int64_t batch, int32_t heads,
+                  int64_t n_q, int32_t head_dim, void* stream) {
+  const char* fn = "attn_finalize";
+  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (n_q < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q must be >= 0", fn);
+  if (batch == 0 || n_q == 0) return ok();
+  if (!l || !o || !out) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned(l, 4) || !aligned(o, 16) || !aligned(out, 16))
+    return fail(Q8A_ERR_MISALIGNED, "%s: l needs 4-byte, o and out 16-byte alignment", fn);
+  cudaError_t e = q8a::launch_finalize(l, o, out, batch, heads, n_q, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+int q8a_device_status(void* stream, uint32_t* status_out, int32_t clear) {
+  uint32_t s = 0;
+  cudaError_t e = q8a::read_device_status(static_cast<cudaStream_t>(stream), &s, clear != 0);
+  if (status_out) *status_out = s;
+  if (e != cudaSuccess) return cuda_fail(e, "q8a_device_status");
+  if (s != 0)
+    return fail(Q8A_ERR_TIMEOUT, "q8a_device_status: a device-side wait ran out (status 0x%x, role %u)",
+                s, (s >> 8) & 0xFFu);
+  return ok();
+}
+
+int q8a_set_wait_timeout_ns(uint64_t ns) {
+  if (ns < 1000000ull) return fail(Q8A_ERR_INVALID_ARG, "q8a_set_wait_timeout_ns: minimum is 1e6 ns");
+  g_timeout_ns.store(ns);
+  return ok();
+}
+
+int q8a_test_inject(int32_t kind) {
+  if (kind != 0 && kind != 1) return fail(Q8A_ERR_INVALID_ARG, "q8a_test_inject: kind must be 0 or 1");
+  g_inject.store(kind);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// internal.h -- launchers shared by the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace q8a {
+
+constexpr int kHeadDim = 64;
+constexpr int kRowBytes = 68;  // one head row: two 34-byte Q8_0 blocks
+
+// q8kv_quantize: fp32 [B][M][H][64] -> Q8_0 planes [B][H] of 68-byte rows.
+cudaError_t launch_quantize(const float* x, uint8_t* out, int64_t batch, int64_t n_tokens,
+                            int32_t heads, int64_t plane_stride, cudaStream_t stream);
+
+// attn_state_init over `rows` = B*H*n_q state rows.
+cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, cudaStream_t stream);
+
+// attn_finalize: fp32 O, l -> fp16 out [B][n_q][H][64].
+cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
+                            int32_t heads, int64_t n_q, cudaStream_t stream);
+
+// Arguments of one chunk-step launch (everything but the Q tensor map).
+struct ChunkArgs {
+  const uint8_t* k8;      // chunk key 0 of plane (0,0)
+  const uint8_t* v8;
+  float* m;
+  float* l;
+  float* o;
+  int64_t plane_stride;   // bytes between (b,h) planes of k8 / v8
+  int64_t q_pos0;         // position of query row 0
+  int64_t kv_start;       // position of chunk key 0
+  int64_t kv_len;         // keys in the chunk (> 0)
+  int64_t n_q;            // query rows per (b,h)
+  int32_t heads;
+  int32_t bh;             // batch * heads
+  int32_t tile0;          // first 128-row query tile launched
+  int32_t n_qtiles;       // query tiles launched per (b,h)
+  float scale;            // logit scale
+  float scale_log2;       // scale * log2(e)
+  int32_t causal;
+  int32_t inject;         // test hook: 1 = first block skips its query-tile load
+  uint64_t timeout_ns;    // budget of every device-side wait
+};
+
+// The tensor map must describe Q as fp16 {H*64, n_q, B} with a {64, 128, 1}
+// box and 128-byte swizzle.
+cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
+
+// Status word of the current device (bit 0: a device-side wait ran out).
+cudaError_t read_device_status(cudaStream_t stream, uint32_t* status, bool clear);
+
+}  // namespace q8a

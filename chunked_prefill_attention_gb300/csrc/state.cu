@@ -1,0 +1,91 @@
+// state.cu -- the persistent online-softmax state before the first chunk and
+// the final normalisation after the last one ("Out-of-Core Flash Streaming &
+// Speculative Decode (1M Context)", §3: m, l, O kept in global memory between
+// chunks; Attention_i = O_i / l_i after chunk C-1).
+//
+// Both kernels are HBM streams: init writes 264 B per (row, head); finalise
+// reads 260 B and writes 128 B.  Finalise maps 8 threads to one 64-float O row
+// (two 128-bit loads each) and writes 8 fp16 (one 128-bit store) per thread, so
+// both the head-major fp32 reads and the token-major fp16 writes are whole
+// 128-byte lines.
+
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace q8a {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+state_init_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
+                  int64_t rows) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  const int64_t start = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = start; i < rows * (kHeadDim / 4); i += stride) o[i] = z;
+  for (int64_t i = start; i < rows; i += stride) {
+    m[i] = -INFINITY;
+    l[i] = 0.0f;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4* __restrict__ out,
+                int64_t n_q, int32_t heads, int64_t rows) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * 8;
+       g += stride) {
+    const int64_t row = g >> 3;         // (b*H + h)*n_q + r
+    const int part = static_cast<int>(g & 7);
+    const int64_t r = row % n_q;
+    const int64_t bh = row / n_q;
+    const int64_t h = bh % heads;
+    const int64_t b = bh / heads;
+    const float lv = __ldg(l + row);
+    const float4 a = __ldg(o + row * 16 + 2 * part);
+    const float4 c = __ldg(o + row * 16 + 2 * part + 1);
+    float y[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = (lv > 0.0f) ? __fdiv_rn(y[i], lv) : 0.0f;
+    uint4 pk;
+    __half2 h0 = __floats2half2_rn(y[0], y[1]);
+    __half2 h1 = __floats2half2_rn(y[2], y[3]);
+    __half2 h2 = __floats2half2_rn(y[4], y[5]);
+    __half2 h3 = __floats2half2_rn(y[6], y[7]);
+    pk.x = *reinterpret_cast<uint32_t*>(&h0);
+    pk.y = *reinterpret_cast<uint32_t*>(&h1);
+    pk.z = *reinterpret_cast<uint32_t*>(&h2);
+    pk.w = *reinterpret_cast<uint32_t*>(&h3);
+    out[((b * n_q + r) * heads + h) * 8 + part] = pk;
+  }
+}
+
+int grid_for(int64_t work) {
+  int64_t blocks = (work + kThreads - 1) / kThreads;
+  const int64_t cap = 152 * 16;   // a few waves of resident blocks; grid-stride beyond
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  state_init_kernel<<<grid_for(rows * 16), kThreads, 0, stream>>>(m, l, reinterpret_cast<float4*>(o),
+                                                                  rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
+                            int32_t heads, int64_t n_q, cudaStream_t stream) {
+  const int64_t rows = batch * heads * n_q;
+  if (rows <= 0) return cudaSuccess;
+  finalize_kernel<<<grid_for(rows * 8), kThreads, 0, stream>>>(
+      l, reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace q8a

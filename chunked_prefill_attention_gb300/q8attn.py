@@ -1,0 +1,182 @@
+"""Python binding of libq8attn.so (ctypes).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors; their device pointers
+and the current torch stream are handed to the C ABI declared in
+include/q8attn.h.  There is no CPU fallback: if the library is missing or fails
+to load, every call raises.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq8attn.so")
+
+Q8A_OK = 0
+Q8A_ERR_INVALID_ARG = -1
+Q8A_ERR_MISALIGNED = -2
+Q8A_ERR_UNSUPPORTED = -3
+Q8A_ERR_CUDA = -4
+Q8A_ERR_TIMEOUT = -5
+ROW_BYTES = 68
+HEAD_DIM = 64
+
+# name -> (restype, argtypes); mirrors include/q8attn.h
+_I64, _I32, _U32, _U64, _P, _F = (ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64,
+                                  ctypes.c_void_p, ctypes.c_float)
+SIGNATURES = {
+    "q8a_abi_version": (_U32, []),
+    "q8a_last_error": (ctypes.c_char_p, []),
+    "q8a_plane_stride_bytes": (_I64, [_I64]),
+    "q8kv_quantize": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _I32, _I64, _P]),
+    "attn_state_init": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
+    "attn_chunk_step": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32,
+                                       _I64, _I32, _F, _I32, _P]),
+    "attn_finalize": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
+    "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
+    "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),
+    "q8a_test_inject": (ctypes.c_int, [_I32]),
+}
+
+_lib = None
+
+
+class Q8AttnError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"q8attn error {code}: {msg}")
+        self.code = code
+
+
+def load():
+    """Load the in-tree shared library (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(rc):
+    if rc != Q8A_OK:
+        raise Q8AttnError(rc, load().q8a_last_error().decode())
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def plane_stride(n_tokens):
+    return int(load().q8a_plane_stride_bytes(n_tokens))
+
+
+def q8kv_quantize(x, out=None, stride=None):
+    """x: fp32 CUDA [B, M, H, 64] -> uint8 [B, H, stride] Q8_0 planes (rows of 68 B)."""
+    B, M, H, D = x.shape
+    if stride is None:
+        stride = plane_stride(M)
+    if out is None:
+        out = torch.empty((B, H, stride), dtype=torch.uint8, device=x.device)
+    _check(load().q8kv_quantize(_ptr(x), _ptr(out), B, M, H, D, stride, _stream(x)))
+    return out
+
+
+class State:
+    """Persistent per-row online-softmax state (fp32): m, l [B, H, n_q]; O [B, H, n_q, 64]."""
+
+    def __init__(self, batch, heads, n_q, device, init=True):
+        self.m = torch.empty((batch, heads, n_q), dtype=torch.float32, device=device)
+        self.l = torch.empty((batch, heads, n_q), dtype=torch.float32, device=device)
+        self.o = torch.empty((batch, heads, n_q, HEAD_DIM), dtype=torch.float32, device=device)
+        if init:
+            attn_state_init(self)
+
+    @property
+    def shape(self):
+        return self.m.shape
+
+
+def attn_state_init(state):
+    B, H, n = state.shape
+    _check(load().attn_state_init(_ptr(state.m), _ptr(state.l), _ptr(state.o), B, H, n, HEAD_DIM,
+                                  _stream(state.m)))
+    return state
+
+
+def attn_chunk_step(q, k8, v8, kv_start, kv_len, state, q_pos0=0, scale=None, causal=True,
+                    stride=None, k_offset_bytes=0):
+    """Fold KV keys [kv_start, kv_start + kv_len) into `state`.
+
+    q: fp16 [B, n_q, H, 64]; k8, v8: uint8 Q8_0 planes [B, H, stride] whose byte
+    `k_offset_bytes` is the chunk's key 0 (so a whole-sequence buffer is passed
+    with k_offset_bytes = kv_start * 68)."""
+    B, n_q, H, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stride is None:
+        stride = k8.shape[-1]
+    lib = load()
+    kp = ctypes.c_void_p(k8.data_ptr() + k_offset_bytes)
+    vp = ctypes.c_void_p(v8.data_ptr() + k_offset_bytes)
+    _check(lib.attn_chunk_step(_ptr(q), q_pos0, kp, vp, stride, kv_start, kv_len, _ptr(state.m),
+                               _ptr(state.l), _ptr(state.o), B, H, n_q, D, scale, int(bool(causal)),
+                               _stream(q)))
+    return state
+
+
+def attn_finalize(state, out=None):
+    """O / l -> fp16 [B, n_q, H, 64]."""
+    B, H, n = state.shape
+    if out is None:
+        out = torch.empty((B, n, H, HEAD_DIM), dtype=torch.float16, device=state.m.device)
+    _check(load().attn_finalize(_ptr(state.l), _ptr(state.o), _ptr(out), B, H, n, HEAD_DIM,
+                                _stream(state.m)))
+    return out
+
+
+def prefill_attention(q, k, v, chunk, scale=None, causal=True, k8=None, v8=None, state=None, out=None):
+    """The whole path: quantise K and V, initialise the state, fold every KV
+    chunk of `chunk` keys in order, finalise.  Returns (out, k8, v8)."""
+    B, M, H, D = q.shape
+    k8 = q8kv_quantize(k, k8)
+    v8 = q8kv_quantize(v, v8)
+    if state is None:
+        state = State(B, H, M, q.device, init=True)
+    else:
+        attn_state_init(state)
+    for s0 in range(0, M, chunk):
+        n = min(chunk, M - s0)
+        attn_chunk_step(q, k8, v8, s0, n, state, scale=scale, causal=causal,
+                        k_offset_bytes=s0 * ROW_BYTES)
+    out = attn_finalize(state, out)
+    return out, k8, v8
+
+
+def device_status(clear=True, stream=None):
+    """(rc, status word) of the current device; synchronises the stream."""
+    st = ctypes.c_uint32(0)
+    s = ctypes.c_void_p(stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    rc = load().q8a_device_status(s, ctypes.byref(st), 1 if clear else 0)
+    return rc, st.value
+
+
+def set_wait_timeout_ns(ns):
+    _check(load().q8a_set_wait_timeout_ns(int(ns)))
+
+
+def test_inject(kind):
+    _check(load().q8a_test_inject(int(kind)))

@@ -1,0 +1,173 @@
+/*
+ * q8attn.h -- C ABI of libq8attn.so: causal FlashAttention prefill over a
+ * Q8_0-quantised KV cache, computed chunk by chunk with a persistent
+ * online-softmax state, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [ARCH]   "Core Architecture & The 4-Brick Pipeline", §5 "Brick 4:
+ *            Barrier-Free FlashAttention & Dynamic Q8_0 KV Cache", part 2
+ *            "Dynamic Q8_0 KV Cache Compression".
+ *   [STREAM] "Out-of-Core Flash Streaming & Speculative Decode (1M Context)",
+ *            §3 "Chunked FlashAttention: Exact Mathematical Derivation" and
+ *            §4 "Mode A vs. Mode B Execution Modes".
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or synchronises on its own; every compute call is
+ *     one or more asynchronous kernel launches on `stream` (a cudaStream_t
+ *     passed as void*; NULL is the legacy default stream).
+ *   - Return value: Q8A_OK (0) or a negative Q8A_ERR_* code.  Arguments are
+ *     validated on the host before any CUDA call, so argument errors are
+ *     reported without touching the device.  q8a_last_error() returns a
+ *     thread-local message for the last failing call of the calling thread.
+ *   - Sizes of zero are allowed and make the call a no-op; negative sizes are
+ *     Q8A_ERR_INVALID_ARG.
+ *   - head_dim must be 64 (two Q8_0 blocks per head row).
+ *   - Layouts (all row-major, contiguous):
+ *       Q, out    fp16  [B][n_q][H][64]          token-major
+ *       x (K, V)  fp32  [B][n_tokens][H][64]     token-major
+ *       K8, V8    Q8_0  [B][H] planes of n_tokens rows of 68 bytes; plane
+ *                 (b, h) starts `plane_stride_bytes * (b*H + h)` bytes after
+ *                 the base.  One 68-byte row = block 0 (channels 0..31) then
+ *                 block 1 (channels 32..63); each 34-byte block is an fp16
+ *                 scale d (little-endian) followed by 32 int8 codes.
+ *       m, l      fp32  [B][H][n_q]
+ *       O         fp32  [B][H][n_q][64]
+ *   - Device wait budget: every wait inside a kernel is bounded (default 2 s,
+ *     see q8a_set_wait_timeout_ns).  A wait that runs out stops the kernel's
+ *     blocks cleanly and records Q8A_ERR_TIMEOUT in a per-device status word
+ *     that q8a_device_status() reads; the CUDA context stays usable.
+ */
+#ifndef Q8ATTN_H_
+#define Q8ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q8A_ABI_VERSION 1u
+
+enum {
+  Q8A_OK = 0,
+  Q8A_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad stride or shape */
+  Q8A_ERR_MISALIGNED = -2,  /* a pointer or stride lacks the required alignment */
+  Q8A_ERR_UNSUPPORTED = -3, /* head_dim other than 64, or a size beyond int32 tiles */
+  Q8A_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
+  Q8A_ERR_TIMEOUT = -5      /* a device-side wait ran out of budget */
+};
+
+#define Q8A_ROW_BYTES 68 /* one 64-channel head row: two 34-byte Q8_0 blocks */
+
+/* ABI version of the loaded library (Q8A_ABI_VERSION). */
+uint32_t q8a_abi_version(void);
+
+/* Thread-local description of the last error returned to this thread ("" if none). */
+const char *q8a_last_error(void);
+
+/* Smallest valid plane stride for n_tokens rows: n_tokens*68 rounded up to 16. */
+int64_t q8a_plane_stride_bytes(int64_t n_tokens);
+
+/*
+ * q8kv_quantize -- dynamic Q8_0 quantisation of one K or V tensor [ARCH].
+ *
+ * For every (b, t, h) row of x and each of its two 32-channel blocks:
+ *   amax = max |x| over the block;  d = fp16_rn(amax / 127)  (IEEE fp32 divide);
+ *   q_i  = round_half_away_from_zero(x_i / d)  (IEEE fp32 divide by the stored
+ *          fp16 d), clamped to [-127, 127];  d == 0 gives all-zero codes.
+ * The result is bit-exact and deterministic.  Inputs must be finite with
+ * |x| <= 65504*127 (larger values are not detected).
+ *
+ *   x                  fp32 [B][n_tokens][H][64], 16-byte aligned.
+ *   q8_out             Q8_0 planes [B][H], row t of plane (b,h) at byte
+ *                      plane_stride*(b*H+h) + 68*t; 16-byte aligned.
+ *   out_plane_stride_bytes  >= n_tokens*68 and a multiple of 16.
+ * Errors: Q8A_ERR_INVALID_ARG, Q8A_ERR_MISALIGNED, Q8A_ERR_UNSUPPORTED, Q8A_ERR_CUDA.
+ */
+int q8kv_quantize(const float *x, void *q8_out, int64_t batch, int64_t n_tokens,
+                  int32_t heads, int32_t head_dim, int64_t out_plane_stride_bytes,
+                  void *stream);
+
+/*
+ * attn_state_init -- the persistent per-row state before the first chunk
+ * [STREAM §3]: m_i = -inf, l_i = 0, O_i = 0 for every (b, h, row).
+ *   m, l  fp32 [B][H][n_q] (4-byte aligned);  o fp32 [B][H][n_q][64] (16-byte aligned).
+ */
+int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
+                    int64_t n_q, int32_t head_dim, void *stream);
+
+/*
+ * attn_chunk_step -- fold one KV chunk into the state [STREAM §3, steps 1-6]:
+ *   S_ij = scale * Q_i . K_j;   m~_i = max_j S_ij;   m'_i = max(m_i, m~_i);
+ *   alpha = e^(m_i - m'_i);     beta_ij = e^(S_ij - m'_i);
+ *   l'_i = alpha*l_i + sum_j beta_ij;   O'_i = alpha*O_i + sum_j beta_ij V_j.
+ * K and V are the dequantised Q8_0 values d*q.  Only visible keys take part:
+ * query row r has position q_pos0 + r, chunk key j has position kv_start + j,
+ * and with `causal` the key is visible iff its position <= the query's (the
+ * triangular mask of [STREAM §4] Mode A).  A row that sees no key of this
+ * chunk keeps its state unchanged; key tiles above the diagonal are skipped
+ * ([ARCH] causal skipping).  Chunks may be folded in any order; the result is
+ * the same up to floating-point rounding.
+ *
+ *   q            fp16 [B][n_q][H][64], 16-byte aligned (rows of this call's queries).
+ *   k_q8, v_q8   key 0 of this chunk in plane (b=0, h=0); plane (b,h) starts
+ *                kv_plane_stride_bytes*(b*H+h) later; 16-byte aligned.
+ *   kv_plane_stride_bytes  >= kv_len*68 and a multiple of 16.  (A slice of a
+ *                whole-sequence Q8_0 buffer uses that buffer's stride and a
+ *                pointer advanced by kv_start*68 bytes, which is 16-byte aligned
+ *                when kv_start is a multiple of 4.)
+ *   kv_start     absolute position of the chunk's first key (>= 0).
+ *   kv_len       number of keys in the chunk (0 makes the call a no-op).
+ *   m, l, o      the state, updated in place (layouts above; o 16-byte aligned).
+ *   scale        logit scale (1/sqrt(64) = 0.125 for the standard model); > 0.
+ *   causal       nonzero for the causal mask, 0 for full (rectangular) attention.
+ * Numerics: Q is fp16; each dequantised key is split exactly into an fp16 high
+ * part and an fp16 residual so that Q.K is formed from exact operands on the
+ * tensor cores with fp32 accumulation; V codes enter the tensor cores exactly
+ * and each V block scale is folded into the fp16 weights beta*d; m, l and O stay
+ * fp32 in the state.
+ * Errors: Q8A_ERR_INVALID_ARG, Q8A_ERR_MISALIGNED, Q8A_ERR_UNSUPPORTED, Q8A_ERR_CUDA.
+ */
+int attn_chunk_step(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,
+                    int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                    float *m, float *l, float *o, int64_t batch, int32_t heads,
+                    int64_t n_q, int32_t head_dim, float scale, int32_t causal,
+                    void *stream);
+
+/*
+ * attn_finalize -- out_i = O_i / l_i after the last chunk [STREAM §3]; a row
+ * with l_i == 0 (it saw no key) gives 0.  out is fp16 (round to nearest even),
+ * [B][n_q][H][64], 16-byte aligned; l 4-byte aligned; o 16-byte aligned.
+ */
+int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int32_t heads,
+                  int64_t n_q, int32_t head_dim, void *stream);
+
+/*
+ * q8a_device_status -- read (and optionally clear) the status word of the
+ * current device: 0 when no device-side wait has run out since the last clear.
+ * Synchronises `stream`.  Returns Q8A_OK, Q8A_ERR_TIMEOUT (when the word is
+ * nonzero; *status_out then holds it: bit 0 set, bits 8..15 the role that gave
+ * up first) or Q8A_ERR_CUDA.  status_out may be NULL.
+ */
+int q8a_device_status(void *stream, uint32_t *status_out, int32_t clear);
+
+/* Budget of every device-side wait, in nanoseconds (default 2e9; minimum 1e6).
+ * Applies to launches made after the call, from any thread. */
+int q8a_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * q8a_test_inject -- test hook for the timeout path.  kind 1 makes the NEXT
+ * attn_chunk_step launch skip the query-tile load (and its barrier arrival) in
+ * its first block, so that block's waits run out, it stops cleanly and the
+ * status word reports Q8A_ERR_TIMEOUT.  kind 0 clears a pending injection.
+ * No memory fault, trap or unbounded wait is involved.
+ */
+int q8a_test_inject(int32_t kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8ATTN_H_ */

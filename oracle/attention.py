@@ -61,15 +61,17 @@ def attention_unchunked(q, k, v, scale, causal=True, q_pos0=0, kv_pos0=0):
     return np.where(any_vis, out, 0.0)
 
 
-def attention_rows(q, k, v, rows, scale, causal=True, q_pos0=0, block=256):
+def attention_rows(q_rows, k, v, rows, scale, causal=True, q_pos0=0, block=256):
     """The plain definition for a subset of query rows (large problems).
 
-    q: [n_q, D] (only `rows` are read); k, v: [n_k, D] with key j at
-    position j.  Rows are processed in blocks; each block only reads the keys
-    up to its largest visible position.  Returns fp64 [len(rows), D].
+    q_rows: [len(rows), D], the queries of `rows`; k, v: [n_k, D] with key j
+    at position j; query row r sits at position q_pos0 + r.  Rows are processed
+    in blocks; each block only reads the keys up to its largest visible
+    position.  Returns fp64 [len(rows), D], in the order of `rows`.
     """
     rows = np.asarray(rows, dtype=np.int64)
-    out = np.zeros((rows.size, q.shape[1]), dtype=np.float64)
+    q_rows = np.asarray(q_rows)
+    out = np.zeros((rows.size, v.shape[1]), dtype=np.float64)
     order = np.argsort(rows, kind="stable")
     for s0 in range(0, rows.size, block):
         idx = order[s0:s0 + block]
@@ -78,7 +80,7 @@ def attention_rows(q, k, v, rows, scale, causal=True, q_pos0=0, block=256):
         if causal:
             n_k = int(min(n_k, q_pos0 + r.max() + 1))
         n_k = max(n_k, 0)
-        qb = np.asarray(q[r], dtype=np.float64)
+        qb = np.asarray(q_rows[idx], dtype=np.float64)
         kb = np.asarray(k[:n_k], dtype=np.float64)
         vb = np.asarray(v[:n_k], dtype=np.float64)
         q_pos = q_pos0 + r

@@ -1,0 +1,124 @@
+"""The C-ABI library builds, loads and exports every symbol that
+include/q8attn.h declares; argument validation answers before any CUDA call.
+Runs without a GPU (no call here reaches a kernel launch)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "q8attn.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_four_calls():
+    names = _declared_functions()
+    for n in ("q8kv_quantize", "attn_state_init", "attn_chunk_step", "attn_finalize"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from chunked_prefill_attention_gb300 import q8attn
+    names = _declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+        assert n in q8attn.SIGNATURES, f"binding lacks {n}"
+    assert lib.q8a_abi_version() == 1
+
+
+def test_plane_stride(lib):
+    assert lib.q8a_plane_stride_bytes(512) == 512 * 68
+    assert lib.q8a_plane_stride_bytes(1) == 80
+    assert lib.q8a_plane_stride_bytes(3) == 208
+    assert lib.q8a_plane_stride_bytes(0) == 0
+    assert lib.q8a_plane_stride_bytes(-1) == -1
+
+
+P = ctypes.c_void_p
+A16 = P(0x100000)     # 16-byte aligned fake addresses: never dereferenced,
+A4 = P(0x100004)      # validation fails before any launch
+
+
+def _err(lib):
+    return lib.q8a_last_error().decode()
+
+
+def test_quantize_validation(lib):
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    s = P(0)
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 32, 272, s) == Q.Q8A_ERR_UNSUPPORTED
+    assert "head_dim" in _err(lib)
+    assert lib.q8kv_quantize(A16, A16, -1, 4, 2, 64, 272, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8kv_quantize(A16, A16, 1, -4, 2, 64, 272, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 0, 64, 272, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8kv_quantize(P(0), A16, 1, 4, 2, 64, 272, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 64, 271, s) == Q.Q8A_ERR_INVALID_ARG   # < 4*68
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 64, 280, s) == Q.Q8A_ERR_MISALIGNED   # % 16
+    assert lib.q8kv_quantize(A4, A16, 1, 4, 2, 64, 288, s) == Q.Q8A_ERR_MISALIGNED
+    # empty problems are no-ops that never touch the device
+    assert lib.q8kv_quantize(A16, A16, 0, 4, 2, 64, 288, s) == Q.Q8A_OK
+    assert lib.q8kv_quantize(P(0), P(0), 1, 0, 2, 64, 0, s) == Q.Q8A_OK
+
+
+def test_state_and_finalize_validation(lib):
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    s = P(0)
+    assert lib.attn_state_init(A16, A16, A16, 1, 2, 8, 128, s) == Q.Q8A_ERR_UNSUPPORTED
+    assert lib.attn_state_init(P(0), A16, A16, 1, 2, 8, 64, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.attn_state_init(A16, A16, A4, 1, 2, 8, 64, s) == Q.Q8A_ERR_MISALIGNED
+    assert lib.attn_state_init(A16, A16, A16, 1, 2, -8, 64, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.attn_state_init(P(0), P(0), P(0), 1, 2, 0, 64, s) == Q.Q8A_OK
+    assert lib.attn_finalize(A16, A16, A4, 1, 2, 8, 64, s) == Q.Q8A_ERR_MISALIGNED
+    assert lib.attn_finalize(A16, P(0), A16, 1, 2, 8, 64, s) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.attn_finalize(P(0), P(0), P(0), 0, 2, 8, 64, s) == Q.Q8A_OK
+
+
+def test_chunk_step_validation(lib):
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    s = P(0)
+
+    def call(q=A16, q_pos0=0, k=A16, v=A16, stride=8704, kv_start=0, kv_len=128, m=A16, l=A16,
+             o=A16, batch=1, heads=2, n_q=128, hd=64, scale=0.125, causal=1):
+        return lib.attn_chunk_step(q, q_pos0, k, v, stride, kv_start, kv_len, m, l, o, batch, heads,
+                                   n_q, hd, scale, causal, s)
+
+    assert call(hd=32) == Q.Q8A_ERR_UNSUPPORTED
+    assert call(k=P(0)) == Q.Q8A_ERR_INVALID_ARG
+    assert call(stride=8703) == Q.Q8A_ERR_INVALID_ARG
+    assert call(stride=8712) == Q.Q8A_ERR_MISALIGNED
+    assert call(k=P(0x100008)) == Q.Q8A_ERR_MISALIGNED
+    assert call(o=A4) == Q.Q8A_ERR_MISALIGNED
+    assert call(scale=0.0) == Q.Q8A_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == Q.Q8A_ERR_INVALID_ARG
+    assert call(kv_start=-1) == Q.Q8A_ERR_INVALID_ARG
+    assert call(q_pos0=-3) == Q.Q8A_ERR_INVALID_ARG
+    assert call(kv_len=-1) == Q.Q8A_ERR_INVALID_ARG
+    # no-ops: empty chunk, no queries, or every query before the chunk (causal)
+    assert call(kv_len=0, k=P(0), v=P(0)) == Q.Q8A_OK
+    assert call(n_q=0) == Q.Q8A_OK
+    assert call(kv_start=128, n_q=128) == Q.Q8A_OK
+
+
+def test_runtime_knobs_validation(lib):
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    assert lib.q8a_set_wait_timeout_ns(10) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8a_set_wait_timeout_ns(2_000_000_000) == Q.Q8A_OK
+    assert lib.q8a_test_inject(7) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8a_test_inject(0) == Q.Q8A_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from chunked_prefill_attention_gb300 import q8attn
+    monkeypatch.setattr(q8attn, "_lib", None)
+    monkeypatch.setattr(q8attn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        q8attn.load()

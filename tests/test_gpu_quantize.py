@@ -1,0 +1,91 @@
+"""q8kv_quantize on the GPU vs the oracle: bit-exact bytes."""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.conftest import cuda_available
+from tests import oracle_runner
+from tests.parity import gpu_bytes, seeded
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+
+def _check(x, lib, stride=None):
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    B, M, H, _ = x.shape
+    out = Q.q8kv_quantize(x, stride=stride)
+    got = gpu_bytes(out, M)
+    want = oracle_runner.quantize_kv(x.cpu().numpy())
+    assert got.shape == want.shape
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        b, h, t, byte = bad[0]
+        raise AssertionError(f"{len(bad)} bytes differ; first at b={b} h={h} t={t} byte={byte}: "
+                             f"gpu {got[b, h, t]} oracle {want[b, h, t]}")
+    return out
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 3, 2), (2, 5, 3), (1, 17, 8), (3, 100, 9),
+                                   (1, 1001, 12), (2, 64, 32), (1, 130, 32)])
+def test_quantize_shapes(lib, shape):
+    B, M, H = shape
+    x = seeded((B, M, H, 64), 100 + M, "cuda")
+    _check(x, lib)
+
+
+def test_quantize_special_values(lib):
+    B, M, H = 1, 64, 8
+    x = seeded((B, M, H, 64), 7, "cuda")
+    x[0, 0] = 0.0                                   # all-zero blocks
+    x[0, 1] *= 1e-6                                 # subnormal fp16 scales
+    x[0, 2] *= 3e-8                                 # scales that underflow to 0
+    x[0, 3] = torch.round(x[0, 3] * 8) / 8          # many exact ties
+    x[0, 4, :, 0] = 127.0                           # d = 1 exactly, ties at .5
+    x[0, 4, :, 1:32] = torch.arange(31, device="cuda", dtype=torch.float32) - 15.5
+    x[0, 5] *= 1000.0                               # large values
+    x[0, 6, :, 5] = -60000.0                        # near the fp16 range
+    x[0, 7] = -x[0, 7].abs()                        # one-signed blocks
+    _check(x, lib)
+
+
+def test_quantize_padded_stride_leaves_padding(lib):
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    B, M, H = 2, 7, 3
+    x = seeded((B, M, H, 64), 9, "cuda")
+    stride = 7 * 68 + 4 + 60        # 540 -> pad to 544 (multiple of 16)
+    stride = (stride + 15) // 16 * 16
+    out = torch.full((B, H, stride), 0xAB, dtype=torch.uint8, device="cuda")
+    Q.q8kv_quantize(x, out=out, stride=stride)
+    assert torch.all(out[:, :, M * 68:] == 0xAB)
+    got = gpu_bytes(out, M)
+    assert np.array_equal(got, oracle_runner.quantize_kv(x.cpu().numpy()))
+
+
+@pytest.mark.parametrize("name", ["m512", "m2k_out", "b8_m2k", "m64k"])
+def test_quantize_workloads_full(lib, name):
+    from chunked_prefill_attention_gb300 import workloads
+    w = workloads.WORKLOADS[name]
+    _, k, v = workloads.make_inputs(w, device="cuda")
+    _check(k, lib)
+    _check(v, lib)
+
+
+def test_quantize_m1m_sampled_windows(lib):
+    """The 1,048,576-token problem: GPU quantises everything; the oracle checks
+    token windows at both ends, around every chunk boundary and at seeded
+    random places (quantisation is independent per row)."""
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads
+    w = workloads.WORKLOADS["m1m"]
+    _, k, v = workloads.make_inputs(w, device="cuda")
+    M = w.tokens
+    g = torch.Generator().manual_seed(w.seed)
+    starts = {0, M - 256} | {c * w.chunk - 128 for c in range(1, w.n_chunks)}
+    starts |= set((torch.randint(0, M - 256, (24,), generator=g) // 16 * 16).tolist())
+    for x in (k, v):
+        out = Q.q8kv_quantize(x)
+        for s0 in sorted(starts):
+            got = out[:, :, s0 * 68:(s0 + 256) * 68].reshape(1, w.heads, 256, 68).cpu().numpy()
+            want = oracle_runner.quantize_kv(x[:, s0:s0 + 256].cpu().numpy())
+            assert np.array_equal(got, want), f"window at token {s0}"
+        del out

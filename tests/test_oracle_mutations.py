@@ -68,7 +68,7 @@ def _attention_pins_pass(am):
     scale = 1 / math.sqrt(d)
     want = _brute(q, k, v, scale)
     for got in (am.attention_unchunked(q, k, v, scale),
-                am.attention_rows(q, k, v, np.arange(n), scale),
+                am.attention_rows(q[::-1], k, v, np.arange(n)[::-1], scale)[::-1],
                 am.attention_chunked(q, k, v, 3, scale),
                 am.attention_chunked(q, k, v, 4, scale, order=[2, 0, 1])):
         if not np.allclose(got, want, atol=1e-12, rtol=0):
