@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark: chunked Q8_0-KV causal prefill attention on GB300.
+
+One step = the whole hot path over one synthetic problem with inputs resident
+in HBM: q8kv_quantize(K), q8kv_quantize(V), attn_state_init, one
+attn_chunk_step per KV chunk (on slices of the whole-sequence Q8_0 buffers),
+attn_finalize.  Default workload: m64k (1 x 65,536 tokens, 32 heads x 64,
+causal, 8 KV chunks of 8,192).
+
+Prints one JSON line (rank 0).  value = causal attention TFLOP/s of the whole
+job: 4*D*B*H*M(M+1)/2 flops per replica per step, summed over ranks, divided
+by the max-over-ranks time of the timed steps.  With --gpus N > 1 every rank
+runs an independent replica (the path does not shard; weak scaling).
+
+--impl reference times the CPU oracle (fp64 numpy, worker pool on the host
+cores) on a bounded prefix of the same workload and prints the same line with
+"impl": "reference".
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal Q8_0-KV prefill attention TFLOP/s & % FP16 tensor peak; tokens/s"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ host side --
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="m64k")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline")
+    p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def dist_barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def dist_max(dist, x):
+    """Max of a float over ranks (identity for one rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def make_record(*, value, n_gpus, steps, warmup, ms_per_step, config, extra):
+    rec = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded torch.randn on the device)",
+        "config": config,
+    }
+    rec.update(extra)
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if mx and s > 0.3 * max(mx)]
+        return {"sm_mhz": statistics.median(busy or sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def profile_traffic(kernel_src):
+    """DRAM bytes per launch of the chunk-step kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "chunk_step_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(kernel_src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec.get("kernel_sha256_16") != h:
+            return None, "stale"
+        return rec, "ok"
+    except Exception:
+        return None, "absent"
+
+
+# ------------------------------------------------------------------ our arm --
+
+def run_ours(args):
+    import torch
+    from chunked_prefill_attention_gb300 import _build, q8attn as Q, workloads as W
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dist = dist_init(world, "nccl")
+    _build.ensure_built()
+    w = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    B, M, H, D = w.batch, w.tokens, w.heads, w.head_dim
+    q, k, v = W.make_inputs(w, device=dev)
+    stride = Q.plane_stride(M)
+    k8 = torch.empty((B, H, stride), dtype=torch.uint8, device=dev)
+    v8 = torch.empty((B, H, stride), dtype=torch.uint8, device=dev)
+    st = Q.State(B, H, M, dev, init=False)
+    out = torch.empty((B, M, H, D), dtype=torch.float16, device=dev)
+    chunks = [(s0, min(w.chunk, M - s0)) for s0 in range(0, M, w.chunk)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        Q.q8kv_quantize(k, k8, stride)
+        Q.q8kv_quantize(v, v8, stride)
+        Q.attn_state_init(st)
+        for i, (s0, n) in enumerate(chunks):
+            if ev is not None:
+                ev[i][0].record(stream)
+            Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * 68)
+            if ev is not None:
+                ev[i][1].record(stream)
+        Q.attn_finalize(st, out)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    rc, status = Q.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in chunks]
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = None if args.no_clocks else ClockSampler(local_rank)
+    dist_barrier(dist)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    t0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(dist)
+    clk = clocks.stop() if clocks else None
+    ms = t0.elapsed_time(t1) / args.steps
+    chunk_ms = sum(a.elapsed_time(b) for per in evs for a, b in per) / args.steps
+    launches_chunk = len(chunks)
+    ms_max = dist_max(dist, ms)
+    rc, status = Q.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {status:#x} after the timed steps")
+
+    flops = w.causal_flops
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    tokens_s = world * B * M / (ms_max * 1e-3)
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_burst = float(peaks.get("bf16_tflops"))
+    achieved = flops / (chunk_ms * 1e-3) / 1e12          # all chunk launches of one step
+    traffic_rec, traffic_state = profile_traffic(
+        os.path.join(ROOT, "chunked_prefill_attention_gb300", "csrc", "chunk_step.cu"))
+    traffic = None
+    if traffic_rec is not None and traffic_rec.get("workload") == w.name:
+        traffic = traffic_rec.get("dram_bytes_per_launch")
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh = q.cpu().pin_memory()
+        kh = k.cpu().pin_memory()
+        vh = v.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            step()
+            oh.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        dist_barrier(dist)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(dist)
+        e_ms = dist_max(dist, a.elapsed_time(b) / args.steps)
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": int(qh.nbytes + kh.nbytes + vh.nbytes),
+               "d2h_bytes_per_step": int(oh.nbytes)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q, k, v, budget_s=20.0)
+
+    n_launch = args.steps * (3 + len(chunks) + 1)
+    config = {
+        "workload": w.describe(), "batch": B, "tokens": M, "heads": H, "head_dim": D,
+        "kv_chunk": w.chunk, "kv_chunks": len(chunks), "replicas": world,
+        "l2": "inputs larger than L2: K, V fp32 %.2f GB, Q fp16 %.2f GB, Q8_0 KV %.2f GB, state %.2f GB"
+              % (2 * k.nbytes / 1e9, q.nbytes / 1e9, 2 * B * H * stride / 1e9,
+                 (st.m.nbytes + st.l.nbytes + st.o.nbytes) / 1e9),
+    }
+    extra = {
+        "tokens_per_s": tokens_s,
+        "pct_fp16_peak": 100.0 * value / (world * peak_sus),
+        "ms_attn_chunks_per_step": chunk_ms,
+        "roofline": {"bound": "tensor", "kernel": "attn_chunk_step", "achieved": achieved,
+                     "peak": peak_sus, "unit": UNIT, "frac": achieved / peak_sus,
+                     "peak_kind": f"dense bf16/fp16 {peak_src} sustained (burst {peak_burst})",
+                     "algorithmic": "4*D flops per unmasked (query, key) pair; %d launches/step" % launches_chunk,
+                     "traffic": traffic, "traffic_note": traffic_state},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": n_launch,
+        "cpu_baseline": cpu,
+    }
+    rec = make_record(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                      ms_per_step=ms_max, config=config, extra=extra)
+    if rank == 0:
+        print(json.dumps(rec), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def _oracle_prefix(qn, kn, vn, n_tok, pool):
+    """Run the oracle's whole path on the first n_tok tokens: quantise K and V,
+    then plain causal attention for every row of every (b, h) plane."""
+    B, M, H, D = qn.shape
+    kq = pool.map(_quant_slice, [kn[:, :n_tok, h:h + 1] for h in range(H)])
+    vq = pool.map(_quant_slice, [vn[:, :n_tok, h:h + 1] for h in range(H)])
+    tasks = []
+    rows = list(range(n_tok))
+    import numpy as np
+    for b in range(B):
+        for h in range(H):
+            tasks.append((qn[b, :n_tok, h].astype(np.float64), np.asarray(rows), kq[h][b, 0], vq[h][b, 0],
+                          1.0 / math.sqrt(D), True, 0))
+    from oracle.runner import _attn_task
+    pool.map(_attn_task, tasks, chunksize=1)
+
+
+def _quant_slice(x):
+    from oracle import q8_0
+    return q8_0.quantize_kv(x)
+
+
+def _oracle_pool():
+    from oracle import runner as oracle_runner
+    return oracle_runner.pool(), oracle_runner.workers()
+
+
+def cpu_baseline(w, q, k, v, budget_s=20.0):
+    """The oracle (as it stands) on the host cores, on a prefix of the
+    workload sized to take about `budget_s` seconds."""
+    pool, cores = _oracle_pool()
+    n_tok = 1024
+    qn = q[:, :min(w.tokens, 16384)].cpu().numpy()
+    kn = k[:, :min(w.tokens, 16384)].cpu().numpy()
+    vn = v[:, :min(w.tokens, 16384)].cpu().numpy()
+    while True:
+        t = time.perf_counter()
+        _oracle_prefix(qn, kn, vn, n_tok, pool)
+        dt = time.perf_counter() - t
+        if dt * 3.5 > budget_s or 2 * n_tok > qn.shape[1]:
+            break
+        n_tok *= 2
+    flops = 4 * w.head_dim * w.batch * w.heads * n_tok * (n_tok + 1) // 2
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"first {n_tok} tokens of {w.name} (all {w.heads} heads): oracle Q8_0 quantise of "
+                      f"K and V + fp64 plain causal attention of every row, numpy, {cores} spawn workers"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from chunked_prefill_attention_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    pool, cores = _oracle_pool()
+    total = max(1, args.steps + args.warmup)
+    n_tok = 2048 if total <= 20 else 1024
+    q, k, v = W.make_inputs(w, device="cpu", tokens=n_tok)
+    qn, kn, vn = q.numpy(), k.numpy(), v.numpy()
+    for _ in range(args.warmup):
+        _oracle_prefix(qn, kn, vn, n_tok, pool)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_prefix(qn, kn, vn, n_tok, pool)
+    dt = (time.perf_counter() - t) / max(args.steps, 1)
+    flops = 4 * w.head_dim * w.batch * w.heads * n_tok * (n_tok + 1) // 2
+    value = flops / dt / 1e12
+    sample = (f"per step: first {n_tok} tokens of {w.name} (all {w.heads} heads): oracle Q8_0 quantise of K "
+              f"and V + fp64 plain causal attention of every row, numpy, {cores} spawn workers")
+    config = {"workload": w.describe(), "batch": w.batch, "tokens": w.tokens, "heads": w.heads,
+              "head_dim": w.head_dim, "kv_chunk": w.chunk, "replicas": 1, "l2": "n/a (host CPU)"}
+    extra = {"impl": "reference", "dtype": "f64",
+             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+             "gpu_launches": 0}
+    rec = make_record(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                      ms_per_step=dt * 1e3, config=config, extra=extra)
+    rec["dtype"] = "f64"
+    rec["data"] = "synthetic (seeded torch.randn on the host)"
+    print(json.dumps(rec), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -37,7 +37,7 @@ struct ChunkArgs {
   int32_t heads;
   int32_t bh;             // batch * heads
   int32_t tile0;          // first 128-row query tile launched
-  int32_t n_qtiles;       // query tiles launched per (b,h)
+  int32_t n_qtiles;       // 128-row query tiles launched per (b,h), from tile0 on
   float scale;            // logit scale
   float scale_log2;       // scale * log2(e)
   int32_t causal;

@@ -1,0 +1,56 @@
+"""Run a few attn_chunk_step launches of a reduced prefill problem, for kernel
+profiling with Nsight Compute.
+
+The problem keeps the m64k draw (Q, K, V ~ N(0,1), seed 3, 32 heads x 64) at
+--tokens tokens split in KV chunks of --chunk keys.  The script quantises K
+and V, initialises the state and folds every chunk once (warm-up), then
+launches the chunk-step kernel for chunk --index another --reps times on the
+same state.  With --tokens 16384 --chunk 8192 --index 1 each profiled launch
+is 64 query tiles x 32 heads over 8,192 keys (a full-tile chunk plus its
+diagonal), and the device holds about 0.3 GB, above the 129 MB L2.
+
+  ncu --set full --clock-control none -k regex:chunk_step_kernel -s 2 -c 1 \\
+      python -m chunked_prefill_attention_gb300.profile_case
+"""
+
+import argparse
+
+
+def main(argv=None):
+    import torch
+
+    from chunked_prefill_attention_gb300 import _build, q8attn as Q, workloads as W
+
+    p = argparse.ArgumentParser()
+    p.add_argument("--tokens", type=int, default=16384)
+    p.add_argument("--chunk", type=int, default=8192)
+    p.add_argument("--index", type=int, default=1)
+    p.add_argument("--reps", type=int, default=2)
+    a = p.parse_args(argv)
+    _build.ensure_built()
+    w = W.WORKLOADS["m64k"]
+    q, k, v = W.make_inputs(w, device="cuda", tokens=a.tokens)
+    B, M, H, _ = q.shape
+    k8 = Q.q8kv_quantize(k)
+    v8 = Q.q8kv_quantize(v)
+    st = Q.State(B, H, M, q.device)
+    starts = list(range(0, M, a.chunk))
+    for s0 in starts:
+        Q.attn_chunk_step(q, k8, v8, s0, min(a.chunk, M - s0), st, k_offset_bytes=s0 * 68)
+    s0 = starts[a.index]
+    n = min(a.chunk, M - s0)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(a.reps):
+        Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * 68)
+    ev[1].record()
+    torch.cuda.synchronize()
+    rc, status = Q.device_status()
+    ms = ev[0].elapsed_time(ev[1]) / a.reps
+    rows = M - (s0 // 128) * 128
+    print(f"chunk {a.index} (keys {s0}..{s0 + n - 1}, query rows {s0 // 128 * 128}..{M - 1}): "
+          f"{ms:.3f} ms per launch, status {rc}")
+
+
+if __name__ == "__main__":
+    main()

@@ -61,13 +61,17 @@ def attention_unchunked(q, k, v, scale, causal=True, q_pos0=0, kv_pos0=0):
     return np.where(any_vis, out, 0.0)
 
 
-def attention_rows(q_rows, k, v, rows, scale, causal=True, q_pos0=0, block=256):
+def attention_rows(q_rows, k, v, rows, scale, causal=True, q_pos0=0, block=256, key_block=16384):
     """The plain definition for a subset of query rows (large problems).
 
     q_rows: [len(rows), D], the queries of `rows`; k, v: [n_k, D] with key j
-    at position j; query row r sits at position q_pos0 + r.  Rows are processed
-    in blocks; each block only reads the keys up to its largest visible
-    position.  Returns fp64 [len(rows), D], in the order of `rows`.
+    at position j; query row r sits at position q_pos0 + r.  Returns fp64
+    [len(rows), D] in the order of `rows`.
+
+    Same two passes as `attention_unchunked` -- first the row maximum over the
+    visible keys, then sum_j e^(s_j - max) and sum_j e^(s_j - max) v_j -- with
+    each pass walking the keys in blocks of `key_block` so that memory stays
+    bounded for very long rows.  Only the order of the fp64 additions differs.
     """
     rows = np.asarray(rows, dtype=np.int64)
     q_rows = np.asarray(q_rows)
@@ -81,19 +85,29 @@ def attention_rows(q_rows, k, v, rows, scale, causal=True, q_pos0=0, block=256):
             n_k = int(min(n_k, q_pos0 + r.max() + 1))
         n_k = max(n_k, 0)
         qb = np.asarray(q_rows[idx], dtype=np.float64)
-        kb = np.asarray(k[:n_k], dtype=np.float64)
-        vb = np.asarray(v[:n_k], dtype=np.float64)
         q_pos = q_pos0 + r
-        k_pos = np.arange(n_k)
-        vis = _visible(q_pos, k_pos, causal)
-        s = np.where(vis, (qb @ kb.T) * scale, -np.inf)
-        m = np.max(s, axis=1, keepdims=True) if n_k else np.full((r.size, 1), -np.inf)
+
+        def scores(k0, k1):
+            kb = np.asarray(k[k0:k1], dtype=np.float64)
+            vis = _visible(q_pos, np.arange(k0, k1), causal)
+            return np.where(vis, (qb @ kb.T) * scale, -np.inf), vis
+
+        m = np.full(r.size, -np.inf)
+        for k0 in range(0, n_k, key_block):            # pass 1: row maximum
+            s, _ = scores(k0, min(n_k, k0 + key_block))
+            m = np.maximum(m, np.max(s, axis=1))
         any_vis = np.isfinite(m)
         m = np.where(any_vis, m, 0.0)
-        p = np.where(vis, np.exp(s - m), 0.0)
-        den = np.sum(p, axis=1, keepdims=True)
-        o = (p @ vb) / np.where(any_vis, den, 1.0)
-        out[idx] = np.where(any_vis, o, 0.0)
+        den = np.zeros(r.size)
+        num = np.zeros((r.size, v.shape[1]))
+        for k0 in range(0, n_k, key_block):            # pass 2: exp-sum and weighted sum
+            k1 = min(n_k, k0 + key_block)
+            s, vis = scores(k0, k1)
+            p = np.where(vis, np.exp(s - m[:, None]), 0.0)
+            den += np.sum(p, axis=1)
+            num += p @ np.asarray(v[k0:k1], dtype=np.float64)
+        o = num / np.where(any_vis, den, 1.0)[:, None]
+        out[idx] = np.where(any_vis[:, None], o, 0.0)
     return out
 
 

@@ -1,6 +1,7 @@
 """Runs the CPU oracle over whole problems, in parallel worker processes.
 
-Test infrastructure: this calls only `oracle/` and numpy.  Worker pools use the
+Test infrastructure (used by tests/, smoke() and the benchmark's CPU-baseline
+leg only): this calls only the oracle modules and numpy.  Worker pools use the
 `spawn` start method so that no worker is forked from a process that already
 holds a CUDA context.  Each task is one (batch, head) plane or one slice of a
 tensor, so the per-task memory stays bounded.
@@ -55,9 +56,7 @@ def _attn_task(args):
     from oracle import q8_0, attention
     k = q8_0.dequantize_kv(k8)
     v = q8_0.dequantize_kv(v8)
-    # bound the score block to ~32 MB of fp64 per step
-    block = int(max(8, min(256, (1 << 22) // max(1, k.shape[0]))))
-    return attention.attention_rows(q_rows, k, v, rows, scale, causal, q_pos0, block=block)
+    return attention.attention_rows(q_rows, k, v, rows, scale, causal, q_pos0, block=256, key_block=8192)
 
 
 def attention(q, k8, v8, scale, causal=True, rows=None, q_pos0=0):

@@ -7,7 +7,7 @@ import numpy as np
 import torch
 
 from chunked_prefill_attention_gb300 import q8attn as Q
-from tests import oracle_runner
+from oracle import runner as oracle_runner
 
 # Attention tolerance: fp16 output with fp32 accumulation against the fp64
 # oracle on identical dequantised KV.
@@ -36,7 +36,14 @@ def run_gpu(q, k, v, chunk, causal=True, scale=None, q_pos0=0, order=None):
         Q.attn_chunk_step(q, k8, v8, s0, min(chunk, M - s0), st, q_pos0=q_pos0, scale=scale,
                           causal=causal, k_offset_bytes=s0 * 68)
     out = Q.attn_finalize(st)
+    assert_device_clean()
     return out, k8, v8, st
+
+
+def assert_device_clean():
+    """No device-side wait ran out since the last check (clears the word)."""
+    rc, status = Q.device_status(clear=True)
+    assert rc == Q.Q8A_OK, f"device status word {status:#x}: a device-side wait ran out"
 
 
 def oracle_out(q, k, v, causal=True, scale=None, rows=None, q_pos0=0):

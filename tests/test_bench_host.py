@@ -1,0 +1,63 @@
+"""Host logic of bench.py for N > 1 (independent replicas): rendezvous,
+barrier, max-over-ranks timing and the whole-job aggregate, run as two `gloo`
+processes on the CPU."""
+
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out_dir):
+    os.environ.update({"RANK": str(rank), "LOCAL_RANK": str(rank), "WORLD_SIZE": str(world),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    r, lr, w = bench.dist_env()
+    assert (r, lr, w) == (rank, rank, world)
+    dist = bench.dist_init(w, "gloo")
+    bench.dist_barrier(dist)
+    # each replica times its own steps; the job's time is the slowest rank's
+    my_ms = 10.0 + 5.0 * rank
+    ms = bench.dist_max(dist, my_ms)
+    flops_per_replica = 1e12
+    value = w * flops_per_replica / (ms * 1e-3) / 1e12
+    rec = bench.make_record(value=value, n_gpus=w, steps=3, warmup=3, ms_per_step=ms,
+                            config={"workload": "test"}, extra={"gpu_launches": 12})
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump(rec, f)
+    dist.destroy_process_group()
+
+
+def test_two_rank_replicas_take_max_time(tmp_path):
+    port = _free_port()
+    mp.start_processes(_worker, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn")
+    recs = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)]
+    for rec in recs:
+        assert rec["ms_per_step"] == 15.0                    # max over ranks
+        assert rec["value"] == pytest.approx(2 * 1e12 / 15e-3 / 1e12)   # whole job
+        assert rec["n_gpus"] == 2 and rec["scaling"] == "weak"
+        for key in ("metric", "unit", "steps", "warmup", "higher_is_better", "vs_baseline",
+                    "dtype", "data", "config"):
+            assert key in rec
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.dist_init(1, "gloo") is None
+    assert bench.dist_max(None, 3.5) == 3.5
+
+
+def test_peaks_fallback(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, src = bench.load_peaks()
+    assert src == "fallback" and peaks["bf16_tflops"] == 1900.0

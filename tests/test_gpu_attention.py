@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from tests.conftest import cuda_available
-from tests.parity import compare, gpu_bytes, oracle_out, run_gpu, seeded
+from tests.parity import assert_device_clean, compare, gpu_bytes, oracle_out, run_gpu, seeded
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
 
@@ -109,6 +109,7 @@ def test_state_checkpoint_resume_bitwise(lib):
     for s0 in (512, 768):
         Q.attn_chunk_step(q, k8, v8, s0, 256, st2, k_offset_bytes=s0 * 68)
     assert torch.equal(Q.attn_finalize(st2), full)
+    assert_device_clean()
 
 
 def test_separate_chunk_buffers_with_ragged_tail(lib):
@@ -122,6 +123,7 @@ def test_separate_chunk_buffers_with_ragged_tail(lib):
         v8 = Q.q8kv_quantize(v[:, s0:s0 + n].contiguous())
         Q.attn_chunk_step(q, k8, v8, s0, n, st)
     out = Q.attn_finalize(st)
+    assert_device_clean()
     want, *_ = oracle_out(q, k, v)
     compare(out.cpu().numpy(), want, "separate buffers")
 
@@ -151,3 +153,4 @@ def test_rows_before_chunk_keep_state(lib):
     assert torch.equal(st.m[:, :, :256], before[0][:, :, :256])
     assert torch.equal(st.l[:, :, :256], before[1][:, :, :256])
     assert torch.equal(st.o[:, :, :256], before[2][:, :, :256])
+    assert_device_clean()

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from tests.conftest import cuda_available
-from tests import oracle_runner
+from oracle import runner as oracle_runner
 from tests.parity import gpu_bytes, seeded
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]

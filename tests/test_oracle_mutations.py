@@ -69,6 +69,7 @@ def _attention_pins_pass(am):
     want = _brute(q, k, v, scale)
     for got in (am.attention_unchunked(q, k, v, scale),
                 am.attention_rows(q[::-1], k, v, np.arange(n)[::-1], scale)[::-1],
+                am.attention_rows(q, k, v, np.arange(n), scale, block=3, key_block=4),
                 am.attention_chunked(q, k, v, 3, scale),
                 am.attention_chunked(q, k, v, 4, scale, order=[2, 0, 1])):
         if not np.allclose(got, want, atol=1e-12, rtol=0):
@@ -91,8 +92,10 @@ ATTN_MUTANTS = [
     ("l not rescaled", "l_new = l_old * alpha + np.sum(beta, axis=1)", "l_new = l_old + np.sum(beta, axis=1)"),
     ("O not rescaled", "o_new = o_old * alpha[:, None] + beta @ v_c", "o_new = o_old + beta @ v_c"),
     ("scale applied twice", "s = (q @ k.T) * scale", "s = (q @ k.T) * scale * scale"),
-    ("row block reads keys transposed", "s = np.where(vis, (qb @ kb.T) * scale, -np.inf)",
-     "s = np.where(vis, (qb @ kb[::-1].T) * scale, -np.inf)"),
+    ("row block reads keys transposed", "return np.where(vis, (qb @ kb.T) * scale, -np.inf), vis",
+     "return np.where(vis, (qb @ kb[::-1].T) * scale, -np.inf), vis"),
+    ("row block drops a key block from the sum", "for k0 in range(0, n_k, key_block):            # pass 2",
+     "for k0 in range(key_block, n_k, key_block):            # pass 2"),
     ("max not subtracted per row", "beta = np.where(vis & live[:, None], np.exp(s - m_safe[:, None]), 0.0)",
      "beta = np.where(vis & live[:, None], np.exp(s - m_safe[None, :1]), 0.0)"),
     ("finalise multiplies", "state[\"O\"] / np.where(pos, l, 1.0)[:, None]", "state[\"O\"] * np.where(pos, l, 1.0)[:, None]"),

@@ -191,6 +191,9 @@ def test_attention_matches_brute_force(m, d, causal, q_pos0):
     assert np.allclose(att.attention_unchunked(q, k, v, scale, causal, q_pos0), want, rtol=0, atol=1e-13)
     rows = np.arange(m)[::-1]
     assert np.allclose(att.attention_rows(q[rows], k, v, rows, scale, causal, q_pos0), want[rows], rtol=0, atol=1e-13)
+    for kb in (1, 2, 3):   # key blocks smaller than the rows: same two-pass result
+        got = att.attention_rows(q[rows], k, v, rows, scale, causal, q_pos0, block=2, key_block=kb)
+        assert np.allclose(got, want[rows], rtol=0, atol=1e-13)
     for c in (1, 2, 3):
         got = att.attention_chunked(q, k, v, c, scale, causal, q_pos0)
         assert np.allclose(got, want, rtol=0, atol=1e-13)
