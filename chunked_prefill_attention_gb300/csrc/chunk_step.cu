@@ -11,32 +11,34 @@
 // skipped (same section, "Causal Skipping").
 //
 // GB300 design.  One CTA = two 128-row query tiles (A, B) of one (batch, head)
-// that share every dequantised key/value tile.  16 warps in four warpgroups:
-//   WG0, WG1   softmax of tile A / tile B (200 registers each after setmaxnreg):
-//              thread i owns query row i of its tile (TMEM lane i), loads its S
-//              row with tcgen05.ld, masks (diagonal and tail tiles only), takes
-//              the row max (3-input max), forms beta = ex2(S*c - m*log2e) with
-//              packed fp32x2 arithmetic, folds the V block scales into the fp16
-//              weights P'_b = fp16(beta * d_b) (so V codes stay exact), writes P'
-//              over its S row, rescales its O row in TMEM when the max moved,
-//              and keeps m and l in registers.  It round-trips (m, l, O) with HBM
-//              before the first and after the last tile.
-//   WG2        dequant (one thread per key row): K = d*q is split exactly into
-//              K_hi = fp16(d*q) and K_lo = fp16(d*q - K_hi) with half2 multiply /
-//              fma on codes converted by the exponent-bias trick, so that
-//              Q.K_hi + Q.K_lo reproduces Q.K from exact fp16 operands; V codes
-//              are converted to fp16 exactly and the two V block scales are kept
-//              aside as fp32.  K tiles are K-major with 128-byte swizzle, V tiles
-//              MN-major with 64-byte swizzle.
+// sharing every dequantised 64-key tile.  16 warps in four warpgroups:
+//   WG0, WG1   softmax of tile A / tile B: thread i owns query row i of its tile
+//              (TMEM lane i).  Per key tile it loads its 64-score S row with
+//              tcgen05.ld, masks (diagonal and tail tiles only), takes the row max
+//              (eight independent 3-input max chains), forms
+//              beta = ex2(S*c - m*log2e) with packed fp32x2 arithmetic, folds the
+//              V block scales into the fp16 weights P'_b = fp16(beta * d_b) (so V
+//              codes stay exact), writes P' over its S row, rescales its O row in
+//              TMEM when the max moved, and keeps m and l in registers.  It
+//              round-trips (m, l, O) with HBM before the first and after the last
+//              key tile.
+//   WG2        dequant, one thread per (key, 32-channel block): K = d*q is split
+//              exactly into K_hi = fp16(d*q) and K_lo = fp16(d*q - K_hi) with
+//              half2 multiply / fma on codes converted by the exponent-bias trick,
+//              so that Q.K_hi + Q.K_lo reproduces Q.K from exact fp16 operands; V
+//              codes become fp16 exactly and the V block scales are kept aside as
+//              fp32.  K tiles are K-major with 128-byte swizzle, V tiles MN-major
+//              with 64-byte swizzle.
 //   WG3        warp 12: producer -- TMA tensor loads of the two fp16 Q tiles and
-//              cp.async.bulk of the raw 68-byte-row K/V tiles (8704 B each,
-//              contiguous in the head-major planes) into a 3-stage ring;
-//              warp 13: MMA issuer (one thread): S_X = Q_X K_hi^T + Q_X K_lo^T
-//              (M=128, N=128, 8 MMAs of K=16) and O_X,b += P'_X,b V_b (M=128,
-//              N=32, A read from TMEM), issued in the order PV_A(t), QK_A(t+1),
-//              PV_B(t), QK_B(t+1) so that each softmax warpgroup works while the
-//              tensor core runs the other tile's MMAs.
-// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384).
+//              cp.async.bulk of the raw 68-byte-row K/V tiles (4352 B each,
+//              contiguous in the head-major planes) into a 4-stage ring;
+//              warp 13: MMA issuer (one thread).  S is double-buffered per query
+//              tile: QK for key tile t+2 goes out right after PV(t) (relying on
+//              tcgen05 MMAs of one thread executing in issue order), so each
+//              softmax warpgroup finds its next S ready and does not wait on the
+//              tensor core, and the issuer only ever waits for P' and K tiles.  S_X = Q_X K_hi^T + Q_X K_lo^T (M=128, N=64, 8 MMAs of
+//              K=16); O_X,b += P'_X,b V_b (M=128, N=32, A read from TMEM).
+// TMEM columns: S[X][buf] at 64*(2X+buf) for X, buf in {0,1}; O_X at 256+64X.
 // Every mbarrier wait is bounded by a wall-clock budget; a wait that runs out
 // records the failing role in a per-device status word, every role then
 // leaves its loop, waits (again bounded) for its own copies / MMAs in flight,
@@ -55,22 +57,19 @@ namespace {
 
 constexpr int BM = 128;                // query rows per tile
 constexpr int NQT = 2;                 // query tiles per CTA
-constexpr int BN = 128;                // keys per tile
-constexpr int RAWB = BN * kRowBytes;   // raw bytes of one K (or V) tile: 8704
-constexpr int NR = 3;                  // raw ring stages
-constexpr int ND = 2;                  // dequantised ring stages
+constexpr int BN = 64;                 // keys per tile
+constexpr int RAWB = BN * kRowBytes;   // raw bytes of one K (or V) tile: 4352
+constexpr int NR = 4;                  // raw ring stages
+constexpr int ND = 4;                  // dequantised ring stages
 constexpr int kThreads = 512;
-constexpr int kRegSoftmax = 200;       // 2 x 128 x 200 + 2 x 128 x 56 = 65536
-constexpr int kRegOther = 56;
-static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split");
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int OFF_Q = 0;                            // NQT x (128 x 128 B), SW128 K-major
-constexpr int DEQ_BYTES = 49152;
-constexpr int DQ_KHI = 0, DQ_KLO = 16384, DQ_V0 = 32768, DQ_V1 = 40960;
+constexpr int OFF_Q = 0;                               // NQT x (128 x 128 B), SW128 K-major
+constexpr int DQ_KHI = 0, DQ_KLO = 8192, DQ_V0 = 16384, DQ_V1 = 20480;
+constexpr int DEQ_BYTES = 24576;                       // K_hi, K_lo (64 x 128 B), V0, V1 (64 x 64 B)
 constexpr int OFF_DEQ = NQT * 16384;
-constexpr int OFF_DV = OFF_DEQ + ND * DEQ_BYTES;    // fp32 V scales [ND][64 pairs][4]
-constexpr int OFF_RAW = OFF_DV + ND * 1024;         // [NR][K raw | V raw]
+constexpr int OFF_DV = OFF_DEQ + ND * DEQ_BYTES;       // fp32 V scales [ND][32 key pairs][4]
+constexpr int OFF_RAW = OFF_DV + ND * 512;             // [NR][K raw | V raw]
 constexpr int OFF_BAR = OFF_RAW + NR * 2 * RAWB;
 // barrier indices
 constexpr int B_QFULL = 0;
@@ -78,20 +77,22 @@ constexpr int B_RAWFULL = 1;                 // NR
 constexpr int B_RAWEMPTY = B_RAWFULL + NR;   // NR
 constexpr int B_DEQFULL = B_RAWEMPTY + NR;   // ND
 constexpr int B_DEQEMPTY = B_DEQFULL + ND;   // ND
-constexpr int B_SFULL = B_DEQEMPTY + ND;     // NQT
-constexpr int B_PFULL = B_SFULL + NQT;       // NQT
+constexpr int B_SFULL = B_DEQEMPTY + ND;     // NQT x 2 buffers
+constexpr int B_PFULL = B_SFULL + 2 * NQT;   // NQT
 constexpr int B_PVDONE = B_PFULL + NQT;      // NQT
 constexpr int B_DRAIN = B_PVDONE + NQT;
 constexpr int NBAR = B_DRAIN + 1;
 constexpr int OFF_CTL = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_CTL + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;        // alignment slack
+constexpr int SMEM_BYTES = SMEM_USED + 1024;           // alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_RAW % 16 == 0 && RAWB % 16 == 0, "bulk copy alignment");
+static_assert(OFF_DEQ % 1024 == 0 && DEQ_BYTES % 1024 == 0, "swizzle atom alignment");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t T_S = 0;      // + 128 * tile
 constexpr uint32_t T_O = 256;    // + 64 * tile
+
+__host__ __device__ constexpr uint32_t s_col(int x, int buf) { return 64u * (2 * x + buf); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -130,15 +131,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl
   }
 }
 
-template <uint32_t N>
-__device__ __forceinline__ void reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -150,12 +142,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
 
@@ -175,7 +165,7 @@ __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<ui
 // Per-CTA work description.
 struct Unit {
   int64_t bh, b, h, r0;   // (batch*heads index), first row of tile A
-  int T[NQT];             // KV tiles each query tile needs (0 = inactive)
+  int T[NQT];             // key tiles each query tile needs (0 = inactive)
   int T_all;              // max over tiles
 };
 
@@ -205,8 +195,9 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
 
 // ------------------------------------------------------------------ roles --
 
-__device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const ChunkArgs& a, const Unit& u,
-                              uint8_t* smem, uint32_t sbase, Ctl* ctl) {
+__device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const ChunkArgs& a,
+                                              const Unit& u, uint8_t* smem, uint32_t sbase,
+                                              Ctl* ctl) {
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
   const bool skip_q = (a.inject == 1) && (blockIdx.x == 0);
@@ -278,9 +269,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
   if (!skip_q) wait_bar(bar(B_QFULL), 0, ctl, a.timeout_ns, R_DRAIN, false);
 }
 
-__device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, uint8_t* smem, uint32_t sbase,
-                             Ctl* ctl) {
-  const int k = threadIdx.x - 256;   // key row of the tile owned by this thread
+__device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, uint8_t* smem,
+                                             uint32_t sbase, Ctl* ctl) {
+  const int tid = threadIdx.x - 256;
+  const int k = tid >> 1;            // key row of the tile
+  const int blk = tid & 1;           // 32-channel block handled by this thread
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
   const int ksw = k & 7;             // 128-byte swizzle phase of this K row
   const int vsw = (k >> 1) & 3;      // 64-byte swizzle phase of this V row
@@ -292,86 +285,72 @@ __device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, 
     const int n_valid = static_cast<int>(i64min(BN, a.kv_len - static_cast<int64_t>(t) * BN));
     uint8_t* dq = smem + OFF_DEQ + sd * DEQ_BYTES;
     // V scales, interleaved per key pair: {d0[2p], d0[2p+1], d1[2p], d1[2p+1]}
-    float* dvs = reinterpret_cast<float*>(smem + OFF_DV + sd * 1024) + (k >> 1) * 4 + (k & 1);
+    float* dvs = reinterpret_cast<float*>(smem + OFF_DV + sd * 512) + (k >> 1) * 4 + 2 * blk + (k & 1);
     uint4* khi_row = reinterpret_cast<uint4*>(dq + DQ_KHI + k * 128);
     uint4* klo_row = reinterpret_cast<uint4*>(dq + DQ_KLO + k * 128);
-    uint8_t* v0_row = dq + DQ_V0 + (k >> 3) * 512 + (k & 7) * 64;
-    uint8_t* v1_row = dq + DQ_V1 + (k >> 3) * 512 + (k & 7) * 64;
+    uint8_t* v_row = dq + (blk ? DQ_V1 : DQ_V0) + (k >> 3) * 512 + (k & 7) * 64;
     if (k < n_valid) {
-      const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + OFF_RAW + sr * 2 * RAWB + k * kRowBytes);
+      // block blk of the key row: bytes 34*blk .. 34*blk+33, inside words 8*blk .. 8*blk+8
+      const uint32_t* rk =
+          reinterpret_cast<const uint32_t*>(smem + OFF_RAW + sr * 2 * RAWB + k * kRowBytes) + 8 * blk;
       const uint32_t* rv = rk + RAWB / 4;
-      // ---- K: block 0 = bytes 0..33 (words 0..8), block 1 = bytes 34..67 (words 8..16)
+      uint32_t w[9];
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        uint32_t w[9];
+      for (int i = 0; i < 9; ++i) w[i] = rk[i];
+      const unsigned short dkb =
+          blk == 0 ? static_cast<unsigned short>(w[0] & 0xFFFFu) : static_cast<unsigned short>(w[0] >> 16);
+      const __half2 d2 = __half2half2(__ushort_as_half(dkb));
 #pragma unroll
-        for (int i = 0; i < 9; ++i) w[i] = rk[8 * blk + i];
-        const unsigned short dbits =
-            blk == 0 ? static_cast<unsigned short>(w[0] & 0xFFFFu) : static_cast<unsigned short>(w[0] >> 16);
-        const __half2 d2 = __half2half2(__ushort_as_half(dbits));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // codes 8c .. 8c+7 of this block
-          uint32_t c0, c1;
-          if (blk == 0) {
-            c0 = __byte_perm(w[2 * c], w[2 * c + 1], 0x5432);
-            c1 = __byte_perm(w[2 * c + 1], w[2 * c + 2], 0x5432);
-          } else {
-            c0 = w[1 + 2 * c];
-            c1 = w[2 + 2 * c];
-          }
-          __half2 q0, q1, q2, q3;
-          codes_to_half2(c0, q0, q1);
-          codes_to_half2(c1, q2, q3);
-          const __half2 h0 = __hmul2(q0, d2), h1 = __hmul2(q1, d2);
-          const __half2 h2 = __hmul2(q2, d2), h3 = __hmul2(q3, d2);
-          const __half2 l0 = __hfma2(q0, d2, __hneg2(h0)), l1 = __hfma2(q1, d2, __hneg2(h1));
-          const __half2 l2 = __hfma2(q2, d2, __hneg2(h2)), l3 = __hfma2(q3, d2, __hneg2(h3));
-          const int pc = (4 * blk + c) ^ ksw;
-          khi_row[pc] = make_uint4(h2u(h0), h2u(h1), h2u(h2), h2u(h3));
-          klo_row[pc] = make_uint4(h2u(l0), h2u(l1), h2u(l2), h2u(l3));
+      for (int c = 0; c < 4; ++c) {
+        // codes 8c .. 8c+7 of this block (block 0 codes start at byte 2, block 1 at byte 36)
+        uint32_t c0, c1;
+        if (blk == 0) {
+          c0 = __byte_perm(w[2 * c], w[2 * c + 1], 0x5432);
+          c1 = __byte_perm(w[2 * c + 1], w[2 * c + 2], 0x5432);
+        } else {
+          c0 = w[1 + 2 * c];
+          c1 = w[2 + 2 * c];
         }
+        __half2 q0, q1, q2, q3;
+        codes_to_half2(c0, q0, q1);
+        codes_to_half2(c1, q2, q3);
+        const __half2 h0 = __hmul2(q0, d2), h1 = __hmul2(q1, d2);
+        const __half2 h2 = __hmul2(q2, d2), h3 = __hmul2(q3, d2);
+        const __half2 l0 = __hfma2(q0, d2, __hneg2(h0)), l1 = __hfma2(q1, d2, __hneg2(h1));
+        const __half2 l2 = __hfma2(q2, d2, __hneg2(h2)), l3 = __hfma2(q3, d2, __hneg2(h3));
+        const int pc = (4 * blk + c) ^ ksw;
+        khi_row[pc] = make_uint4(h2u(h0), h2u(h1), h2u(h2), h2u(h3));
+        klo_row[pc] = make_uint4(h2u(l0), h2u(l1), h2u(l2), h2u(l3));
       }
-      // ---- V: codes to fp16 (exact), scales aside
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        uint32_t w[9];
+      for (int i = 0; i < 9; ++i) w[i] = rv[i];
+      const unsigned short dvb =
+          blk == 0 ? static_cast<unsigned short>(w[0] & 0xFFFFu) : static_cast<unsigned short>(w[0] >> 16);
+      *dvs = __half2float(__ushort_as_half(dvb));
 #pragma unroll
-        for (int i = 0; i < 9; ++i) w[i] = rv[8 * blk + i];
-        const unsigned short dbits =
-            blk == 0 ? static_cast<unsigned short>(w[0] & 0xFFFFu) : static_cast<unsigned short>(w[0] >> 16);
-        dvs[2 * blk] = __half2float(__ushort_as_half(dbits));
-        uint8_t* vrow = blk == 0 ? v0_row : v1_row;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t c0, c1;
-          if (blk == 0) {
-            c0 = __byte_perm(w[2 * c], w[2 * c + 1], 0x5432);
-            c1 = __byte_perm(w[2 * c + 1], w[2 * c + 2], 0x5432);
-          } else {
-            c0 = w[1 + 2 * c];
-            c1 = w[2 + 2 * c];
-          }
-          __half2 q0, q1, q2, q3;
-          codes_to_half2(c0, q0, q1);
-          codes_to_half2(c1, q2, q3);
-          *reinterpret_cast<uint4*>(vrow + 16 * (c ^ vsw)) = make_uint4(h2u(q0), h2u(q1), h2u(q2), h2u(q3));
+      for (int c = 0; c < 4; ++c) {
+        uint32_t c0, c1;
+        if (blk == 0) {
+          c0 = __byte_perm(w[2 * c], w[2 * c + 1], 0x5432);
+          c1 = __byte_perm(w[2 * c + 1], w[2 * c + 2], 0x5432);
+        } else {
+          c0 = w[1 + 2 * c];
+          c1 = w[2 + 2 * c];
         }
+        __half2 q0, q1, q2, q3;
+        codes_to_half2(c0, q0, q1);
+        codes_to_half2(c1, q2, q3);
+        *reinterpret_cast<uint4*>(v_row + 16 * (c ^ vsw)) = make_uint4(h2u(q0), h2u(q1), h2u(q2), h2u(q3));
       }
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        khi_row[c] = z;
-        klo_row[c] = z;
-      }
-#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        *reinterpret_cast<uint4*>(v0_row + 16 * c) = z;
-        *reinterpret_cast<uint4*>(v1_row + 16 * c) = z;
+        khi_row[4 * blk + c] = z;
+        klo_row[4 * blk + c] = z;
+        *reinterpret_cast<uint4*>(v_row + 16 * c) = z;
       }
-      dvs[0] = 0.0f;
-      dvs[2] = 0.0f;
+      *dvs = 0.0f;
     }
     fence_proxy_async_smem();
     mbar_arrive(bar(B_DEQFULL + sd));
@@ -379,16 +358,16 @@ __device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, 
   }
 }
 
-__device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint32_t sbase, uint32_t tmem,
-                         Ctl* ctl) {
+__device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint32_t sbase,
+                                         uint32_t tmem, Ctl* ctl) {
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
-  constexpr uint32_t kIdescQK = idesc_f16_f32(128, 128, 0, 0);
+  constexpr uint32_t kIdescQK = idesc_f16_f32(128, BN, 0, 0);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, 32, 0, 1);
 
   auto issue_qk = [&](int x, int t) {
     const uint32_t dq = sbase + OFF_DEQ + (t % ND) * DEQ_BYTES;
-    const uint32_t d_tmem = tmem + T_S + 128 * x;
+    const uint32_t d_tmem = tmem + s_col(x, t & 1);
     const uint32_t qa = sbase + OFF_Q + x * 16384;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
@@ -403,76 +382,90 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
   };
   auto issue_pv = [&](int x, int t) {
     const uint32_t dq = sbase + OFF_DEQ + (t % ND) * DEQ_BYTES;
-    const uint32_t p_tmem = tmem + T_S + 128 * x;
+    const uint32_t p_tmem = tmem + s_col(x, t & 1);
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
       const uint32_t vb = dq + (blk ? DQ_V1 : DQ_V0);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < BN / 16; ++kk) {
         const uint64_t bd = smem_desc(vb + 1024 * kk, 512, 512, kSwizzle64);
-        mma_ts(tmem + T_O + 64 * x + 32 * blk, p_tmem + 64 * blk + 8 * kk, bd, kIdescPV, 1u);
+        mma_ts(tmem + T_O + 64 * x + 32 * blk, p_tmem + 32 * blk + 8 * kk, bd, kIdescPV, 1u);
       }
     }
   };
 
+  // Event-driven issue: lane 0 polls the barriers without blocking and issues
+  // whatever is ready, so one query tile's softmax never waits behind the other's.
+  //   PV_x(t)   once tile x has written P'(t)            (p_full[x], phase t)
+  //   QK_x(t)   once key tile t is dequantised (deq_full) and PV_x(t-2) has been
+  //             issued: QK_x(t) reuses the S buffer PV_x(t-2) reads P' from, and
+  //             MMAs issued by one thread execute in issue order
+  //   stage r   released (deq_empty) once every query tile has issued PV(r)
   bool ok = wait_bar(bar(B_QFULL), 0, ctl, a.timeout_ns, R_MMA, true);
-  if (ok) ok = wait_bar(bar(B_DEQFULL + 0), 0, ctl, a.timeout_ns, R_MMA, true);
-  if (ok) {
-    if (lane == 0) {
-      tc_fence_after();
+  if (ok && lane == 0) {
+    int pv_next[NQT], qk_next[NQT];
 #pragma unroll
-      for (int x = 0; x < NQT; ++x)
-        if (u.T[x] > 0) {
-          issue_qk(x, 0);
-          mma_commit(bar(B_SFULL + x));
-        }
-    }
-    __syncwarp();
-    for (int t = 0; t < u.T_all && ok; ++t) {
+    for (int x = 0; x < NQT; ++x) pv_next[x] = qk_next[x] = 0;
+    int released = 0;
+    uint64_t last = global_timer_ns();
+    int idle = 0;
+    while (true) {
+      bool progress = false;
 #pragma unroll
       for (int x = 0; x < NQT; ++x) {
-        if (t >= u.T[x]) continue;
-        if (!wait_bar(bar(B_PFULL + x), t & 1, ctl, a.timeout_ns, R_MMA, true)) {
-          ok = false;
+        const int tp = pv_next[x];
+        if (tp < u.T[x] && mbar_test_wait(bar(B_PFULL + x), tp & 1)) {
+          tc_fence_after();
+          issue_pv(x, tp);
+          mma_commit(bar(B_PVDONE + x));
+          pv_next[x] = tp + 1;
+          progress = true;
+        }
+        const int tq = qk_next[x];
+        if (tq < u.T[x] && tq - 2 < pv_next[x] &&
+            mbar_test_wait(bar(B_DEQFULL + tq % ND), (tq / ND) & 1)) {
+          tc_fence_after();
+          issue_qk(x, tq);
+          mma_commit(bar(B_SFULL + 2 * x + (tq & 1)));
+          qk_next[x] = tq + 1;
+          progress = true;
+        }
+      }
+      int lowest = u.T_all;
+#pragma unroll
+      for (int x = 0; x < NQT; ++x)
+        if (pv_next[x] < u.T[x]) lowest = min(lowest, pv_next[x]);
+      while (released < lowest) {
+        mma_commit(bar(B_DEQEMPTY + released % ND));
+        ++released;
+        progress = true;
+      }
+      if (released >= u.T_all) break;   // every PV issued and every stage released
+      if (progress) {
+        idle = 0;
+        last = global_timer_ns();
+      } else if (++idle > 8) {
+        if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort) != 0u) break;
+        const uint64_t now = global_timer_ns();
+        if (now - last > a.timeout_ns) {
+          *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
+          atomicCAS(&g_status, 0u, 1u | (R_MMA << 8));
           break;
         }
-        if (lane == 0) {
-          tc_fence_after();
-          issue_pv(x, t);
-          mma_commit(bar(B_PVDONE + x));
-          // release the dequantised stage after the last PV that reads it
-          bool last = true;
-#pragma unroll
-          for (int y = x + 1; y < NQT; ++y) last = last && (t >= u.T[y]);
-          if (last) mma_commit(bar(B_DEQEMPTY + t % ND));
-        }
-        __syncwarp();
-        if (t + 1 < u.T[x]) {
-          // K of tile t+1 dequantised, and S_x no longer read as P' by PV_x(t)
-          if (!wait_bar(bar(B_DEQFULL + (t + 1) % ND), ((t + 1) / ND) & 1, ctl, a.timeout_ns, R_MMA,
-                        true) ||
-              !wait_bar(bar(B_PVDONE + x), t & 1, ctl, a.timeout_ns, R_MMA, true)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            tc_fence_after();
-            issue_qk(x, t + 1);
-            mma_commit(bar(B_SFULL + x));
-          }
-          __syncwarp();
-        }
+        __nanosleep(32);
       }
     }
   }
+  __syncwarp();
   // Never leave with an MMA in flight.
   if (lane == 0) mma_commit(bar(B_DRAIN));
   __syncwarp();
   wait_bar(bar(B_DRAIN), 0, ctl, a.timeout_ns, R_DRAIN, false);
 }
 
-__device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, int x, uint8_t* smem,
-                             uint32_t sbase, uint32_t tmem, Ctl* ctl) {
+__device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, int x,
+                                             uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                                             Ctl* ctl) {
   const int row = threadIdx.x & 127;       // TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;   // warp's lane quarter
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -484,73 +477,75 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
   const int64_t pos = a.q_pos0 + rg;
   const bool active = rg < a.n_q && (!a.causal || pos >= a.kv_start);
   const int64_t sidx = u.bh * a.n_q + rg;
-  const uint32_t t_s = tmem + lane_off + T_S + 128 * x;
   const uint32_t t_o = tmem + lane_off + T_O + 64 * x;
 
   float m_run = -INFINITY, l_run = 0.0f;
-  {
-    uint32_t oa[32], ob[32];
+  if (active) {
+    m_run = a.m[sidx];
+    l_run = a.l[sidx];
+  }
+  // the O row enters TMEM in two 32-column halves
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t oh[32];
     if (active) {
-      m_run = a.m[sidx];
-      l_run = a.l[sidx];
-      const float4* src = reinterpret_cast<const float4*>(a.o + sidx * kHeadDim);
+      const float4* src = reinterpret_cast<const float4*>(a.o + sidx * kHeadDim) + 8 * half;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float4 p = src[i];
-        oa[4 * i + 0] = __float_as_uint(p.x);
-        oa[4 * i + 1] = __float_as_uint(p.y);
-        oa[4 * i + 2] = __float_as_uint(p.z);
-        oa[4 * i + 3] = __float_as_uint(p.w);
-        const float4 y = src[8 + i];
-        ob[4 * i + 0] = __float_as_uint(y.x);
-        ob[4 * i + 1] = __float_as_uint(y.y);
-        ob[4 * i + 2] = __float_as_uint(y.z);
-        ob[4 * i + 3] = __float_as_uint(y.w);
+        oh[4 * i + 0] = __float_as_uint(p.x);
+        oh[4 * i + 1] = __float_as_uint(p.y);
+        oh[4 * i + 2] = __float_as_uint(p.z);
+        oh[4 * i + 3] = __float_as_uint(p.w);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) oa[i] = ob[i] = 0u;
+      for (int i = 0; i < 32; ++i) oh[i] = 0u;
     }
-    tmem_st32(t_o, oa);
-    tmem_st32(t_o + 32, ob);
-    tmem_wait_st();
+    tmem_st32(t_o + 32 * half, oh);
   }
+  tmem_wait_st();
 
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int64_t q_first = a.q_pos0 + u.r0 + x * BM;   // position of the tile's first row
   bool ok = true;
   for (int t = 0; t < T; ++t) {
     const int sd = t % ND;
-    if (!wait_bar(bar(B_SFULL + x), t & 1, ctl, a.timeout_ns, R_SOFTMAX, true) ||
+    const uint32_t t_s = tmem + lane_off + s_col(x, t & 1);
+    if (!wait_bar(bar(B_SFULL + 2 * x + (t & 1)), (t >> 1) & 1, ctl, a.timeout_ns, R_SOFTMAX, true) ||
         !wait_bar(bar(B_DEQFULL + sd), (t / ND) & 1, ctl, a.timeout_ns, R_SOFTMAX, true)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    uint32_t s[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(t_s + 32 * c, s[c]);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_wait_ld(s[c]);
+    uint32_t s[2][32];
+    tmem_ld32(t_s, s[0]);
+    tmem_ld32(t_s + 32, s[1]);
+    tmem_wait_ld(s[0]);
+    tmem_wait_ld(s[1]);
 
     const int64_t k0 = static_cast<int64_t>(t) * BN;
-    const bool need_mask = (k0 + BN > a.kv_len) ||
-                           (a.causal && a.kv_start + k0 + BN - 1 > a.q_pos0 + u.r0 + x * BM);
+    const bool need_mask = (k0 + BN > a.kv_len) || (a.causal && a.kv_start + k0 + BN - 1 > q_first);
     if (need_mask) {
       int64_t lim = a.kv_len - 1 - k0;
       if (a.causal) lim = i64min(lim, pos - a.kv_start - k0);
       const int li = static_cast<int>(i64max(-1, i64min(lim, BN - 1)));
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (32 * c + j > li) s[c][j] = __float_as_uint(-INFINITY);
     }
-    float mx = -INFINITY;
+    // row max over 64 scores: eight independent 3-input chains, then combine
+    float pm[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; j += 2)
-        mx = max3(mx, __uint_as_float(s[c][j]), __uint_as_float(s[c][j + 1]));
+    for (int p = 0; p < 32; ++p) {       // key pair p = keys 2p, 2p+1
+      const int j = 2 * p;
+      pm[p & 7] = max3(pm[p & 7], __uint_as_float(s[j >> 5][j & 31]), __uint_as_float(s[j >> 5][(j & 31) + 1]));
+    }
+    const float mx = fmaxf(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], max3(pm[5], pm[6], pm[7])));
     const float m_new = fmaxf(m_run, mx * a.scale);
     float alpha = 1.0f, mlog = 0.0f;
     if (m_new != -INFINITY) {
@@ -558,25 +553,28 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
       mlog = m_new * kLog2e;
     }
     const float2 nm2 = make_float2(-mlog, -mlog);
-    const float4* dv = reinterpret_cast<const float4*>(smem + OFF_DV + sd * 1024);
-    float2 rs = make_float2(0.0f, 0.0f);
+    const float4* dv = reinterpret_cast<const float4*>(smem + OFF_DV + sd * 512);
+    float2 rs[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t pa[16], pb[16];
+    for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const float2 sv = make_float2(__uint_as_float(s[c][2 * jj]), __uint_as_float(s[c][2 * jj + 1]));
+    for (int g = 0; g < 4; ++g) {          // 16 keys per group
+      uint32_t pa[8], pb[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = 16 * g + 2 * jj;     // key pair (j, j+1)
+        const float2 sv = make_float2(__uint_as_float(s[j >> 5][j & 31]), __uint_as_float(s[j >> 5][(j & 31) + 1]));
         const float2 e = __ffma2_rn(sv, sl2, nm2);
         const float2 bt = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-        rs = __fadd2_rn(rs, bt);
-        const float4 d = dv[16 * c + jj];
+        rs[jj & 3] = __fadd2_rn(rs[jj & 3], bt);
+        const float4 d = dv[j >> 1];
         const float2 p0 = __fmul2_rn(bt, make_float2(d.x, d.y));
         const float2 p1 = __fmul2_rn(bt, make_float2(d.z, d.w));
         pa[jj] = pack_half2(p0.x, p0.y);
         pb[jj] = pack_half2(p1.x, p1.y);
       }
-      tmem_st16(t_s + 16 * c, pa);
-      tmem_st16(t_s + 64 + 16 * c, pb);
+      tmem_st8(t_s + 8 * g, pa);          // P'_0: columns [0, 32)
+      tmem_st8(t_s + 32 + 8 * g, pb);     // P'_1: columns [32, 64)
     }
     if (t > 0) {
       if (!wait_bar(bar(B_PVDONE + x), (t - 1) & 1, ctl, a.timeout_ns, R_SOFTMAX, true)) {
@@ -586,48 +584,46 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
       tc_fence_after();
     }
     if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-      uint32_t oa[32], ob[32];
-      tmem_ld32(t_o, oa);
-      tmem_ld32(t_o + 32, ob);
-      tmem_wait_ld(oa);
-      tmem_wait_ld(ob);
       const float2 al = make_float2(alpha, alpha);
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        float2 va = __fmul2_rn(make_float2(__uint_as_float(oa[i]), __uint_as_float(oa[i + 1])), al);
-        float2 vb = __fmul2_rn(make_float2(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), al);
-        oa[i] = __float_as_uint(va.x);
-        oa[i + 1] = __float_as_uint(va.y);
-        ob[i] = __float_as_uint(vb.x);
-        ob[i + 1] = __float_as_uint(vb.y);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t oh[32];
+        tmem_ld32(t_o + 32 * half, oh);
+        tmem_wait_ld(oh);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 v = __fmul2_rn(make_float2(__uint_as_float(oh[i]), __uint_as_float(oh[i + 1])), al);
+          oh[i] = __float_as_uint(v.x);
+          oh[i + 1] = __float_as_uint(v.y);
+        }
+        tmem_st32(t_o + 32 * half, oh);
       }
-      tmem_st32(t_o, oa);
-      tmem_st32(t_o + 32, ob);
     }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(bar(B_PFULL + x));
-    l_run = fmaf(l_run, alpha, rs.x + rs.y);   // same ops per tile with or without chunking
+    const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+    l_run = fmaf(l_run, alpha, r.x + r.y);   // same ops per tile with or without chunking
     m_run = m_new;
   }
   if (ok) {
     if (wait_bar(bar(B_PVDONE + x), (T - 1) & 1, ctl, a.timeout_ns, R_SOFTMAX, true)) {
       tc_fence_after();
-      uint32_t oa[32], ob[32];
-      tmem_ld32(t_o, oa);
-      tmem_ld32(t_o + 32, ob);
-      tmem_wait_ld(oa);
-      tmem_wait_ld(ob);
       if (active) {
         a.m[sidx] = m_run;
         a.l[sidx] = l_run;
-        float4* dst = reinterpret_cast<float4*>(a.o + sidx * kHeadDim);
+      }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          dst[i] = make_float4(__uint_as_float(oa[4 * i]), __uint_as_float(oa[4 * i + 1]),
-                               __uint_as_float(oa[4 * i + 2]), __uint_as_float(oa[4 * i + 3]));
-          dst[8 + i] = make_float4(__uint_as_float(ob[4 * i]), __uint_as_float(ob[4 * i + 1]),
-                                   __uint_as_float(ob[4 * i + 2]), __uint_as_float(ob[4 * i + 3]));
+      for (int half = 0; half < 2; ++half) {
+        uint32_t oh[32];
+        tmem_ld32(t_o + 32 * half, oh);
+        tmem_wait_ld(oh);
+        if (active) {
+          float4* dst = reinterpret_cast<float4*>(a.o + sidx * kHeadDim) + 8 * half;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(oh[4 * i]), __uint_as_float(oh[4 * i + 1]),
+                                 __uint_as_float(oh[4 * i + 2]), __uint_as_float(oh[4 * i + 3]));
         }
       }
     }
@@ -668,22 +664,17 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   const uint32_t tmem = ctl->tmem_base;
 
   if (wg < 2) {
-    reg_alloc<kRegSoftmax>();
     softmax_role(a, u, wg, smem, sbase, tmem, ctl);
-    tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
-    return;
-  }
-  reg_dealloc<kRegOther>();
-  if (wg == 2) {
+  } else if (wg == 2) {
     dequant_role(a, u, smem, sbase, ctl);
   } else if (warp == 12) {
     producer_role(&qmap, a, u, smem, sbase, ctl);
   } else if (warp == 13) {
     mma_role(a, u, sbase, tmem, ctl);
   }
+
   tc_fence_before();
-  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  __syncthreads();
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
