@@ -15,10 +15,7 @@ import numpy as np
 _POOL = None
 
 
-def _init_worker():
-    # one BLAS thread per worker: the pool itself supplies the parallelism
-    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[v] = "1"
+_BLAS_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
 def workers():
@@ -26,9 +23,22 @@ def workers():
 
 
 def pool():
+    """One BLAS thread per worker: the pool itself supplies the parallelism.
+    The limit must be in the environment when a worker starts, because the
+    worker imports numpy (and so sizes its BLAS thread pool) while it unpickles
+    its task function, before any initializer runs."""
     global _POOL
     if _POOL is None:
-        _POOL = mp.get_context("spawn").Pool(workers(), initializer=_init_worker)
+        saved = {v: os.environ.get(v) for v in _BLAS_VARS}
+        os.environ.update({v: "1" for v in _BLAS_VARS})
+        try:
+            _POOL = mp.get_context("spawn").Pool(workers())
+        finally:
+            for v, old in saved.items():
+                if old is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = old
     return _POOL
 
 
