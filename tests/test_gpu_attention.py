@@ -83,16 +83,22 @@ def test_chunk_order_any(lib):
         assert torch.max(torch.abs(out.float() - ref.float())).item() < 2e-3
 
 
-def test_chunked_equals_single_chunk_bitwise(lib):
-    """With chunk boundaries on 128-key tile boundaries the per-row operations
-    are identical, so the state and output are bit-identical."""
+def test_chunked_matches_single_chunk(lib):
+    """Folding the keys in one chunk or in several gives the same state: the
+    running max m bit for bit (the same fp32 scores in the same key tiles); l
+    and O up to the rounding of the fp16 weights, whose exponent reference a
+    chunk boundary resets to the running max while a single chunk may keep an
+    older one; outputs within the parity tolerance."""
     q, k, v = _inputs(2, 1024, 3, seed=71)
     a, *_, sa = run_gpu(q, k, v, 1024)
-    b, *_, sb = run_gpu(q, k, v, 256)
-    c, *_, sc = run_gpu(q, k, v, 128)
-    assert torch.equal(a, b) and torch.equal(a, c)
-    for x, y in ((sa, sb), (sa, sc)):
-        assert torch.equal(x.m, y.m) and torch.equal(x.l, y.l) and torch.equal(x.o, y.o)
+    want, *_ = oracle_out(q, k, v)
+    for chunk in (256, 128):
+        b, *_, sb = run_gpu(q, k, v, chunk)
+        compare(b.cpu().numpy(), want, f"chunk {chunk}")
+        assert torch.equal(sa.m, sb.m)
+        assert torch.allclose(sa.l, sb.l, rtol=1e-3, atol=0)
+        assert torch.allclose(sa.o / sa.l[..., None], sb.o / sb.l[..., None], rtol=0, atol=2e-3)
+        assert torch.max(torch.abs(a.float() - b.float())).item() <= 2e-3
 
 
 def test_state_checkpoint_resume_bitwise(lib):
