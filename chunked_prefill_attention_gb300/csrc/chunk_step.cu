@@ -15,17 +15,15 @@
 //   WG0, WG1   softmax of tile A / tile B.  Thread i owns query row i of its
 //              tile (TMEM lane i).  Per key tile it loads its whole 128-score S
 //              row from TMEM into registers, masks diagonal and tail tiles,
-//              takes the row max, forms beta = ex2(S*c - m_ref*log2e) with
-//              packed fp32x2 arithmetic, writes P = fp16(beta) over the
-//              first 64 columns of its S row and adds those fp16 weights into
-//              l in fp32 (so O / l is a convex combination under exactly the
-//              weights the tensor cores used).
-//              Rescaling is lazy: the exponent reference m_ref moves (and O and
-//              l are multiplied by alpha) only when the row max exceeds m_ref by
-//              more than 8*ln2, so beta <= 256 and most tiles never touch O.
-//              The true running max is tracked alongside; before writing the
-//              state back, O and l are rescaled to it, so the state in HBM is
-//              the recurrence's (m, l, O) exactly.
+//              takes the row max, forms beta = ex2(S*c - m*log2e) with packed
+//              fp32x2 arithmetic against the running max m (so the weight of
+//              the row's largest score is exactly 1), sums beta in fp32 and
+//              writes P = fp16(beta) over the first 64 columns of its S row, in
+//              two halves (keys 0-63, then 64-127) announced on separate
+//              barriers so that the first half of PV runs while the second
+//              half is computed.  A warp rescales its O rows in TMEM, before
+//              the first half is announced, only when the max of one of its
+//              rows moved.
 //   WG2        dequant, one thread per key row.  K = d*q and V = d*q are each
 //              split exactly into an fp16 high part fp16(d*q) and an fp16
 //              residual fp16(d*q - high) (half2 multiply / fma on codes
@@ -36,7 +34,8 @@
 //   WG3        warp 12: producer -- TMA tensor loads of the two fp16 Q tiles and
 //              cp.async.bulk of the raw 68-byte-row K/V tiles (8704 B each,
 //              contiguous in the head-major planes) into a 2-stage ring;
-//              warp 13: MMA issuer (one thread).
+//              warp 13: MMA issuer (the whole warp runs the issue loop, so the
+//              descriptors stay warp-uniform; one elected lane issues).
 // MMAs (M=128, K=16, N=128 throughout: N=128 is the narrowest shape that runs
 // at the tensor pipe's full rate on this part):
 //   S_X  = Q_X K_hi^T + Q_X K_lo^T          8 instructions, both operands in smem
@@ -87,8 +86,8 @@ constexpr int B_RAWEMPTY = B_RAWFULL + NR;   // NR
 constexpr int B_DEQFULL = B_RAWEMPTY + NR;   // ND
 constexpr int B_DEQEMPTY = B_DEQFULL + ND;   // ND
 constexpr int B_SFULL = B_DEQEMPTY + ND;     // NQT
-constexpr int B_PFULL = B_SFULL + NQT;       // NQT
-constexpr int B_ODONE = B_PFULL + NQT;       // NQT
+constexpr int B_PFULL = B_SFULL + NQT;       // 2 x NQT: P_x keys 0-63, then keys 64-127
+constexpr int B_ODONE = B_PFULL + 2 * NQT;   // NQT
 constexpr int B_DRAIN = B_ODONE + NQT;
 constexpr int NBAR = B_DRAIN + 1;
 constexpr int OFF_CTL = OFF_BAR + NBAR * 8;
@@ -103,7 +102,6 @@ constexpr uint32_t T_S = 0;      // + 128 * tile
 constexpr uint32_t T_O = 256;    // + 128 * tile; high half at +0, residual half at +64
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kTau = 5.545177444479562f;   // 8 ln 2: rescale threshold, beta <= 2^8
 
 // role ids recorded in the status word when a wait runs out
 enum : uint32_t { R_SOFTMAX = 1, R_DEQUANT = 2, R_PRODUCER = 3, R_MMA = 4, R_DRAIN = 5 };
@@ -147,18 +145,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl
     }
     stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
     if (stop) return false;
-  }
-}
-
-// The same for a single thread (the MMA issuer).
-__device__ __forceinline__ bool wait_bar1(uint32_t bar, uint32_t parity, Ctl* ctl,
-                                          uint64_t budget_cycles, uint32_t role, bool honour_abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-    if (honour_abort && *reinterpret_cast<volatile uint32_t*>(&ctl->abort) != 0u) return false;
-    if (budget_ran_out(ctl, t0, budget_cycles, role)) return false;
   }
 }
 
@@ -206,16 +192,6 @@ __device__ __forceinline__ void tmem_st32_at(uint32_t taddr, const uint32_t (&r)
       "%29, %30, %31, %32};" ::"r"(taddr),
       Q8A_W8(r, O + 0), Q8A_W8(r, O + 8), Q8A_W8(r, O + 16), Q8A_W8(r, O + 24)
       : "memory");
-}
-
-// acc0 += lo half of h, acc1 += hi half of h (mixed-precision fp16 + fp32 adds).
-__device__ __forceinline__ void add_half2_to(float& acc0, float& acc1, uint32_t h) {
-  asm("{\n\t.reg .f16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "add.rn.f32.f16 %0, lo, %0;\n\t"
-      "add.rn.f32.f16 %1, hi, %1;\n\t}"
-      : "+f"(acc0), "+f"(acc1)
-      : "r"(h));
 }
 
 // Four signed int8 codes -> two half2 (exact): flip the sign bit to get
@@ -415,87 +391,113 @@ __device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, 
   }
 }
 
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// The whole warp runs the issue loop, so every descriptor and TMEM address is
+// warp-uniform and stays in uniform registers; one elected lane issues the
+// MMAs and commits (always the same lane: commits track its own MMAs).
 __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint32_t sbase,
                                          uint32_t tmem, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;   // cycles
-  const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, BN, 0, 0);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, 0, 1);
+  const bool leader = elect_one();
 
-  // S_x = Q_x K_hi^T + Q_x K_lo^T: K-major operands, 4 k-steps of 16 channels
-  // (32 bytes inside the 128-byte swizzled rows).
+  // Descriptor start addresses advance in 16-byte units in the low bits (no
+  // carry: shared addresses stay below 256 KB).
+  //   S_x = Q_x K_hi^T + Q_x K_lo^T: K-major operands, 4 k-steps of 16 channels
+  //   (32 bytes inside the 128-byte swizzled rows).
+  //   O_x += P_x [V_hi | V_lo]: V tiles MN-major (channels contiguous); the two
+  //   64-channel halves of N are 16 KB apart (leading byte offset) and each
+  //   k-step covers 16 keys = two 8-row swizzle atoms (stride byte offset 1 KB,
+  //   2 KB per k-step).  P of keys 16kk .. 16kk+15 sits in TMEM columns
+  //   8kk .. 8kk+7 of S_x.
+  const uint64_t qdesc0 = smem_desc(sbase + OFF_Q, 1024, 1024, kSwizzle128);
+  const uint64_t kdesc0 = smem_desc(sbase + OFF_DEQ + DQ_KHI, 1024, 1024, kSwizzle128);
+  const uint64_t vdesc0 = smem_desc(sbase + OFF_DEQ + DQ_VHI, DQ_VLO - DQ_VHI, 1024, kSwizzle128);
   auto issue_qk = [&](int x, int t) {
-    const uint32_t dq = sbase + OFF_DEQ + (t % ND) * DEQ_BYTES;
-    const uint32_t qa = sbase + OFF_Q + x * 16384;
+    const uint64_t qd = qdesc0 + static_cast<uint64_t>(x * (16384 >> 4));
+    const uint64_t kd = kdesc0 + static_cast<uint64_t>((t % ND) * (DEQ_BYTES >> 4));
+    const uint32_t d = tmem + T_S + 128u * x;
+    if (leader) {
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      const uint32_t kb = dq + (part ? DQ_KLO : DQ_KHI);
+      for (int part = 0; part < 2; ++part)
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = smem_desc(qa + 32 * kk, 1024, 1024, kSwizzle128);
-        const uint64_t bd = smem_desc(kb + 32 * kk, 1024, 1024, kSwizzle128);
-        mma_ss(tmem + T_S + 128u * x, ad, bd, kIdescQK, (part | kk) != 0 ? 1u : 0u);
-      }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(d, qd + 2 * kk, kd + part * (16384 >> 4) + 2 * kk, kIdescQK, (part | kk) != 0 ? 1u : 0u);
     }
   };
-  // O_x += P_x [V_hi | V_lo]: V tiles are MN-major (channels contiguous); the
-  // two 64-channel halves of N are 16 KB apart (leading byte offset) and each
-  // k-step covers 16 keys = two 8-row swizzle atoms (stride byte offset 1 KB).
-  // P of keys 16kk .. 16kk+15 sits in TMEM columns 8kk .. 8kk+7 of S_x.
-  auto issue_pv = [&](int x, int t) {
-    const uint32_t vb = sbase + OFF_DEQ + (t % ND) * DEQ_BYTES + DQ_VHI;
+  // half h covers keys 64h .. 64h+63 (k-steps 4h .. 4h+3)
+  auto issue_pv = [&](int x, int t, int h) {
+    const uint64_t vd = vdesc0 + static_cast<uint64_t>((t % ND) * (DEQ_BYTES >> 4));
+    const uint32_t o = tmem + T_O + 128u * x;
+    const uint32_t p = tmem + T_S + 128u * x;
+    if (leader) {
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-      const uint64_t bd = smem_desc(vb + 2048 * kk, DQ_VLO - DQ_VHI, 1024, kSwizzle128);
-      mma_ts(tmem + T_O + 128u * x, tmem + T_S + 128u * x + 8u * kk, bd, kIdescPV, 1u);
+      for (int kk = 4 * h; kk < 4 * h + 4; ++kk) mma_ts(o, p + 8u * kk, vd + 128 * kk, kIdescPV, 1u);
     }
+  };
+  auto commit = [&](int b) {
+    if (leader) mma_commit(bar(b));
   };
 
-  if (lane == 0) {
-    bool ok = wait_bar1(bar(B_QFULL), 0, ctl, budget, R_MMA, true) &&
-              wait_bar1(bar(B_DEQFULL + 0), 0, ctl, budget, R_MMA, true);
-    if (ok) {
-      tc_fence_after();
+  bool ok = wait_bar(bar(B_QFULL), 0, ctl, budget, R_MMA, true) &&
+            wait_bar(bar(B_DEQFULL + 0), 0, ctl, budget, R_MMA, true);
+  if (ok) {
+    tc_fence_after();
 #pragma unroll
-      for (int x = 0; x < NQT; ++x)
-        if (u.T[x] > 0) {
-          issue_qk(x, 0);
-          mma_commit(bar(B_SFULL + x));
+    for (int x = 0; x < NQT; ++x)
+      if (u.T[x] > 0) {
+        issue_qk(x, 0);
+        commit(B_SFULL + x);
+      }
+  }
+  int deq_ready = 0;   // highest key tile whose dequantised stage is known full
+  for (int t = 0; ok && t < u.T_all; ++t) {
+#pragma unroll
+    for (int x = 0; x < NQT; ++x) {
+      if (t < u.T[x]) {
+        if (!wait_bar(bar(B_PFULL + 2 * x), t & 1, ctl, budget, R_MMA, true)) {
+          ok = false;
+          break;
         }
-    }
-    int deq_ready = 0;   // highest key tile whose dequantised stage is known full
-    for (int t = 0; ok && t < u.T_all; ++t) {
-#pragma unroll
-      for (int x = 0; x < NQT; ++x) {
-        if (t < u.T[x]) {
-          if (!wait_bar1(bar(B_PFULL + x), t & 1, ctl, budget, R_MMA, true)) {
+        tc_fence_after();
+        issue_pv(x, t, 0);
+        if (!wait_bar(bar(B_PFULL + 2 * x + 1), t & 1, ctl, budget, R_MMA, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(x, t, 1);
+        if (t == u.T[x] - 1) commit(B_ODONE + x);
+      }
+      if (x == NQT - 1) commit(B_DEQEMPTY + t % ND);   // every reader of tile t issued
+      if (t + 1 < u.T[x]) {
+        if (deq_ready < t + 1) {
+          if (!wait_bar(bar(B_DEQFULL + (t + 1) % ND), ((t + 1) / ND) & 1, ctl, budget, R_MMA,
+                        true)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(x, t);
-          if (t == u.T[x] - 1) mma_commit(bar(B_ODONE + x));
+          deq_ready = t + 1;
         }
-        if (x == NQT - 1) mma_commit(bar(B_DEQEMPTY + t % ND));   // every reader of tile t issued
-        if (t + 1 < u.T[x]) {
-          if (deq_ready < t + 1) {
-            if (!wait_bar1(bar(B_DEQFULL + (t + 1) % ND), ((t + 1) / ND) & 1, ctl, budget, R_MMA,
-                           true)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            deq_ready = t + 1;
-          }
-          issue_qk(x, t + 1);
-          mma_commit(bar(B_SFULL + x));
-        }
+        issue_qk(x, t + 1);
+        commit(B_SFULL + x);
       }
     }
-    // Never leave with an MMA in flight.
-    mma_commit(bar(B_DRAIN));
   }
+  // Never leave with an MMA in flight.
+  commit(B_DRAIN);
   __syncwarp();
   wait_bar(bar(B_DRAIN), 0, ctl, budget, R_DRAIN, false);
 }
@@ -517,14 +519,11 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
   const uint32_t t_s = tmem + lane_off + T_S + 128u * x;
   const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
 
-  // m_true: the running max of the recurrence; m_ref: the reference l and O are
-  // currently scaled to (m_true - kTau <= m_ref <= m_true).
-  float m_true = -INFINITY, l_run = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;
   if (active) {
-    m_true = a.m[sidx];
+    m_run = a.m[sidx];
     l_run = a.l[sidx];
   }
-  float m_ref = m_true;
   {
     // the O row enters TMEM as the high half; the residual half starts at 0
     uint32_t oh[64];
@@ -573,7 +572,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
 
     const int64_t k0 = static_cast<int64_t>(t) * BN;
     const bool need_mask = (k0 + BN > a.kv_len) || (a.causal && a.kv_start + k0 + BN - 1 > q_first);
-    if (need_mask) {
+    if (__builtin_expect(need_mask, 0)) {
       int64_t lim = a.kv_len - 1 - k0;
       if (a.causal) lim = i64min(lim, pos - a.kv_start - k0);
       const int li = static_cast<int>(i64max(-1, i64min(lim, BN - 1)));
@@ -589,61 +588,76 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
       pm[p & 7] = max3(pm[p & 7], __uint_as_float(s[2 * p]), __uint_as_float(s[2 * p + 1]));
     const float mx = fmaxf(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], max3(pm[5], pm[6], pm[7])));
     const float t_nat = mx * a.scale;   // -inf when every key of the tile is masked
-    m_true = fmaxf(m_true, t_nat);
     float alpha = 1.0f;
-    const bool resc = t_nat > m_ref + kTau;   // always true for the first visible key
+    const bool resc = t_nat > m_run;      // the running max moves
     if (resc) {
-      alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx((m_ref - m_true) * kLog2e);
-      m_ref = m_true;
+      alpha = (m_run == -INFINITY) ? 0.0f : ex2_approx((m_run - t_nat) * kLog2e);
+      m_run = t_nat;
     }
-    const float mlog = (m_ref == -INFINITY) ? 0.0f : m_ref * kLog2e;
+    const float mlog = (m_run == -INFINITY) ? 0.0f : m_run * kLog2e;
     const float2 nm2 = make_float2(-mlog, -mlog);
-    // l sums the fp16 weights that PV uses, so the normalised output is an
-    // exact convex combination of the values under the rounded weights.
-    float rs[8];
+    float2 rs[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
+    for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.0f, 0.0f);
+    // P for keys 0-63 (TMEM columns 0-31), then keys 64-127 (columns 32-63);
+    // each half is announced on its own barrier so that the first half of
+    // PV_x(t) runs while the second half is being computed.
     uint32_t p[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
+    for (int i = 0; i < 32; ++i) {
       const float2 sv = make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
       const float2 e = __ffma2_rn(sv, sl2, nm2);
-      p[i] = pack_half2(ex2_approx(e.x), ex2_approx(e.y));
-      add_half2_to(rs[2 * (i & 3)], rs[2 * (i & 3) + 1], p[i]);
+      const float2 bt = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+      rs[i & 3] = __fadd2_rn(rs[i & 3], bt);
+      p[i] = pack_half2(bt.x, bt.y);
     }
     tmem_st32_at<0>(t_s, p);
-    tmem_st32_at<32>(t_s + 32, p);
-    // PV_x(t-1) has completed (QK_x(t), issued after it, has), so O is stable.
+    // PV_x(t-1) has completed (QK_x(t), issued after it, has), so O is stable;
+    // it is rescaled before the first half of PV_x(t) accumulates into it,
+    // 64 columns (the high then the residual half) per round.
     if (__any_sync(0xFFFFFFFFu, resc)) {
       const float2 al = make_float2(alpha, alpha);
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t oh[32];
-        tmem_ld32(t_o + 32 * q4, oh);
-        tmem_wait_ld(oh);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o[64];
+        tmem_ld32(t_o + 64 * hh, *reinterpret_cast<uint32_t (*)[32]>(&o[0]));
+        tmem_ld32(t_o + 64 * hh + 32, *reinterpret_cast<uint32_t (*)[32]>(&o[32]));
+        tmem_wait_ld(*reinterpret_cast<uint32_t (*)[32]>(&o[0]));
+        tmem_wait_ld(*reinterpret_cast<uint32_t (*)[32]>(&o[32]));
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 v = __fmul2_rn(make_float2(__uint_as_float(oh[i]), __uint_as_float(oh[i + 1])), al);
-          oh[i] = __float_as_uint(v.x);
-          oh[i + 1] = __float_as_uint(v.y);
+        for (int i = 0; i < 64; i += 2) {
+          const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al);
+          o[i] = __float_as_uint(v.x);
+          o[i + 1] = __float_as_uint(v.y);
         }
-        tmem_st32(t_o + 32 * q4, oh);
+        tmem_st32_at<0>(t_o + 64 * hh, o);
+        tmem_st32_at<32>(t_o + 64 * hh + 32, o);
       }
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(bar(B_PFULL + x));
-    const float r = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-    l_run = fmaf(l_run, alpha, r);
+    mbar_arrive(bar(B_PFULL + 2 * x));
+#pragma unroll
+    for (int i = 32; i < 64; ++i) {
+      const float2 sv = make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+      const float2 e = __ffma2_rn(sv, sl2, nm2);
+      const float2 bt = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+      rs[i & 3] = __fadd2_rn(rs[i & 3], bt);
+      p[i] = pack_half2(bt.x, bt.y);
+    }
+    tmem_st32_at<32>(t_s + 32, p);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar(B_PFULL + 2 * x + 1));
+    const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+    l_run = fmaf(l_run, alpha, r.x + r.y);   // same ops per tile with or without chunking
   }
   if (ok) {
     if (wait_bar(bar(B_ODONE + x), 0, ctl, budget, R_SOFTMAX, true)) {
       tc_fence_after();
-      // back to the recurrence's reference: l and O scaled to the running max
-      const float f = (m_ref == m_true) ? 1.0f : ex2_approx((m_ref - m_true) * kLog2e);
       if (active) {
-        a.m[sidx] = m_true;
-        a.l[sidx] = l_run * f;
+        a.m[sidx] = m_run;
+        a.l[sidx] = l_run;
       }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -659,7 +673,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
             float v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              v[e] = (__uint_as_float(oh[4 * i + e]) + __uint_as_float(ol[4 * i + e])) * f;
+              v[e] = __uint_as_float(oh[4 * i + e]) + __uint_as_float(ol[4 * i + e]);
             dst[i] = make_float4(v[0], v[1], v[2], v[3]);
           }
         }
@@ -686,7 +700,7 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
       uint32_t count = 1;
       if (i >= B_RAWEMPTY && i < B_RAWEMPTY + NR) count = 128;   // dequant threads
       if (i >= B_DEQFULL && i < B_DEQFULL + ND) count = 128;     // dequant threads
-      if (i >= B_PFULL && i < B_PFULL + NQT) count = 128;        // softmax threads of a tile
+      if (i >= B_PFULL && i < B_PFULL + 2 * NQT) count = 128;    // softmax threads of a tile
       mbar_init(sbase + OFF_BAR + 8u * i, count);
     }
     ctl->abort = 0u;

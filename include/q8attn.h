@@ -123,11 +123,11 @@ int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
  *   m, l, o      the state, updated in place (layouts above; o 16-byte aligned).
  *   scale        logit scale (1/sqrt(64) = 0.125 for the standard model); > 0.
  *   causal       nonzero for the causal mask, 0 for full (rectangular) attention.
- * Numerics: Q is fp16; each dequantised key is split exactly into an fp16 high
- * part and an fp16 residual so that Q.K is formed from exact operands on the
- * tensor cores with fp32 accumulation; V codes enter the tensor cores exactly
- * and each V block scale is folded into the fp16 weights beta*d; m, l and O stay
- * fp32 in the state.
+ * Numerics: Q is fp16; each dequantised key and value d*q is split exactly
+ * into an fp16 high part and an fp16 residual, so Q.K and P.V are formed from
+ * exact operands on the tensor cores with fp32 accumulation; the weights
+ * P = e^(S - m) are rounded to fp16 once, against the running max m (the
+ * largest weight of a row is exactly 1); m, l and O stay fp32 in the state.
  * Errors: Q8A_ERR_INVALID_ARG, Q8A_ERR_MISALIGNED, Q8A_ERR_UNSUPPORTED, Q8A_ERR_CUDA.
  */
 int attn_chunk_step(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,

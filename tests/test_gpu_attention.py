@@ -84,20 +84,18 @@ def test_chunk_order_any(lib):
 
 
 def test_chunked_matches_single_chunk(lib):
-    """Folding the keys in one chunk or in several gives the same state: the
-    running max m bit for bit (the same fp32 scores in the same key tiles); l
-    and O up to the rounding of the fp16 weights, whose exponent reference a
-    chunk boundary resets to the running max while a single chunk may keep an
-    older one; outputs within the parity tolerance."""
+    """With chunk boundaries on 128-key tile boundaries every row sees the same
+    fp32 scores in the same key tiles, so m and l are bit-identical whether the
+    keys come in one chunk or several.  O differs only in where its high and
+    residual accumulator halves are added (at each chunk boundary), i.e. by
+    fp32 rounding."""
     q, k, v = _inputs(2, 1024, 3, seed=71)
     a, *_, sa = run_gpu(q, k, v, 1024)
-    want, *_ = oracle_out(q, k, v)
     for chunk in (256, 128):
         b, *_, sb = run_gpu(q, k, v, chunk)
-        compare(b.cpu().numpy(), want, f"chunk {chunk}")
-        assert torch.equal(sa.m, sb.m)
-        assert torch.allclose(sa.l, sb.l, rtol=1e-3, atol=0)
-        assert torch.allclose(sa.o / sa.l[..., None], sb.o / sb.l[..., None], rtol=0, atol=2e-3)
+        assert torch.equal(sa.m, sb.m) and torch.equal(sa.l, sb.l)
+        diff = (sa.o - sb.o).abs() / sa.l[..., None]
+        assert diff.max().item() <= 1e-5
         assert torch.max(torch.abs(a.float() - b.float())).item() <= 2e-3
 
 
