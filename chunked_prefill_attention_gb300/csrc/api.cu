@@ -107,17 +107,25 @@ int attn_state_init(float* m, float* l, float* o, int64_t batch, int32_t heads, 
   return ok();
 }
 
-int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
-                    int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
-                    float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
-                    float scale, int32_t causal, void* stream) {
-  const char* fn = "attn_chunk_step";
+namespace {
+
+// Validation, query-tile range and Q tensor map shared by the two chunk-step
+// entry points.  Returns Q8A_OK with *empty set when the call has nothing to do.
+int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void* k_q8,
+                       const void* v_q8, int64_t kv_plane_stride_bytes, int64_t kv_start,
+                       int64_t kv_len, float* m, float* l, float* o, int64_t batch, int32_t heads,
+                       int64_t n_q, int32_t head_dim, float scale, int32_t causal,
+                       CUtensorMap* qmap, q8a::ChunkArgs* a, bool* empty) {
+  *empty = false;
   if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
   if (n_q < 0 || kv_len < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q and kv_len must be >= 0", fn);
   if (q_pos0 < 0 || kv_start < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: positions must be >= 0", fn);
   if (!(scale > 0.0f) || !std::isfinite(scale))
     return fail(Q8A_ERR_INVALID_ARG, "%s: scale must be finite and > 0", fn);
-  if (batch == 0 || n_q == 0 || kv_len == 0) return ok();
+  if (batch == 0 || n_q == 0 || kv_len == 0) {
+    *empty = true;
+    return Q8A_OK;
+  }
   if (!q || !k_q8 || !v_q8 || !m || !l || !o) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (kv_plane_stride_bytes < kv_len * Q8A_ROW_BYTES)
     return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < kv_len*68 = %lld", fn,
@@ -133,7 +141,10 @@ int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void*
   int64_t first_row = 0;
   if (causal) {
     first_row = kv_start - q_pos0;
-    if (first_row >= n_q) return ok();   // every query precedes the chunk
+    if (first_row >= n_q) {   // every query precedes the chunk
+      *empty = true;
+      return Q8A_OK;
+    }
     if (first_row < 0) first_row = 0;
   }
   const int64_t tile0 = first_row / 128;
@@ -143,40 +154,109 @@ int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void*
 
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
-  CUtensorMap qmap;
-  std::memset(&qmap, 0, sizeof(qmap));
+  std::memset(qmap, 0, sizeof(*qmap));
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(heads) * 64, static_cast<cuuint64_t>(n_q),
                               static_cast<cuuint64_t>(batch)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * 64 * 2,
                                  static_cast<cuuint64_t>(heads) * 64 * 2 * static_cast<cuuint64_t>(n_q)};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult cr = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q), dims, strides,
+  CUresult cr = enc(qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", fn, (int)cr);
 
-  q8a::ChunkArgs a{};
-  a.k8 = static_cast<const uint8_t*>(k_q8);
-  a.v8 = static_cast<const uint8_t*>(v_q8);
-  a.m = m;
-  a.l = l;
-  a.o = o;
-  a.plane_stride = kv_plane_stride_bytes;
-  a.q_pos0 = q_pos0;
-  a.kv_start = kv_start;
-  a.kv_len = kv_len;
-  a.n_q = n_q;
-  a.heads = heads;
-  a.bh = static_cast<int32_t>(batch * heads);
-  a.tile0 = static_cast<int32_t>(tile0);
-  a.n_qtiles = static_cast<int32_t>(n_qtiles);
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.causal = causal ? 1 : 0;
+  *a = q8a::ChunkArgs{};
+  a->k8 = static_cast<const uint8_t*>(k_q8);
+  a->v8 = static_cast<const uint8_t*>(v_q8);
+  a->m = m;
+  a->l = l;
+  a->o = o;
+  a->plane_stride = kv_plane_stride_bytes;
+  a->q_pos0 = q_pos0;
+  a->kv_start = kv_start;
+  a->kv_len = kv_len;
+  a->n_q = n_q;
+  a->heads = heads;
+  a->bh = static_cast<int32_t>(batch * heads);
+  a->tile0 = static_cast<int32_t>(tile0);
+  a->n_qtiles = static_cast<int32_t>(n_qtiles);
+  a->scale = scale;
+  a->scale_log2 = scale * 1.4426950408889634f;
+  a->causal = causal ? 1 : 0;
+  a->timeout_ns = g_timeout_ns.load();
+  return Q8A_OK;
+}
+
+}  // namespace
+
+int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                    int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
+                    float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
+                    float scale, int32_t causal, void* stream) {
+  const char* fn = "attn_chunk_step";
+  CUtensorMap qmap;
+  q8a::ChunkArgs a;
+  bool empty = false;
+  if (int rc = prepare_chunk_step(fn, q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start,
+                                  kv_len, m, l, o, batch, heads, n_q, head_dim, scale, causal,
+                                  &qmap, &a, &empty))
+    return rc;
+  if (empty) return ok();
   a.inject = g_inject.exchange(0);
-  a.timeout_ns = g_timeout_ns.load();
   cudaError_t e = q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
+                                   int64_t split_keys) {
+  if (batch < 0 || heads <= 0 || n_q < 0 || kv_len < 0 || split_keys <= 0) return -1;
+  const int64_t n_splits = (kv_len + split_keys - 1) / split_keys;
+  return n_splits * batch * heads * n_q * (Q8A_HEAD_DIM + 2);
+}
+
+int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                          int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                          float* m, float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
+                          int32_t head_dim, float scale, int32_t causal, int64_t split_keys,
+                          float* workspace, int64_t workspace_floats, void* stream) {
+  const char* fn = "attn_chunk_step_split";
+  if (split_keys <= 0 || split_keys % 128 != 0)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
+                fn, (long long)split_keys);
+  // the workspace is checked before anything touches the device
+  int64_t n_splits = 0, rows = 0;
+  if (batch > 0 && heads > 0 && n_q > 0 && kv_len > 0) {
+    n_splits = (kv_len + split_keys - 1) / split_keys;
+    if (n_splits > 65535) return fail(Q8A_ERR_UNSUPPORTED, "%s: more than 65535 key ranges", fn);
+    rows = batch * heads * n_q;
+    const int64_t need = n_splits * rows * (Q8A_HEAD_DIM + 2);
+    if (!workspace) return fail(Q8A_ERR_INVALID_ARG, "%s: null workspace", fn);
+    if (workspace_floats < need)
+      return fail(Q8A_ERR_INVALID_ARG, "%s: workspace of %lld floats < %lld needed", fn,
+                  (long long)workspace_floats, (long long)need);
+    if (!aligned(workspace, 16))
+      return fail(Q8A_ERR_MISALIGNED, "%s: workspace needs 16-byte alignment", fn);
+  }
+  CUtensorMap qmap;
+  q8a::ChunkArgs a;
+  bool empty = false;
+  if (int rc = prepare_chunk_step(fn, q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start,
+                                  kv_len, m, l, o, batch, heads, n_q, head_dim, scale, causal,
+                                  &qmap, &a, &empty))
+    return rc;
+  if (empty) return ok();
+  // workspace: partial O [n_splits][rows][64], then m [n_splits][rows], then l
+  a.split_keys = split_keys;
+  a.n_splits = static_cast<int32_t>(n_splits);
+  a.part_o = workspace;
+  a.part_m = workspace + n_splits * rows * Q8A_HEAD_DIM;
+  a.part_l = a.part_m + n_splits * rows;
+  a.inject = g_inject.exchange(0);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = q8a::launch_chunk_step(qmap, a, st);
+  if (e == cudaSuccess) e = q8a::launch_split_merge(a, st);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }

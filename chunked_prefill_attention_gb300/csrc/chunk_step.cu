@@ -207,6 +207,43 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, __half2& lo, __half2&
 }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// The key range and state this CTA works on: the whole chunk and the state,
+// or, in the split form, one key range and its partial state.
+struct Range {
+  int64_t kv_len, kv_start;
+  const uint8_t* k8;
+  const uint8_t* v8;
+  float* m;
+  float* l;
+  float* o;
+  bool fresh;   // start from the empty state instead of reading m, l, o
+};
+
+__device__ __forceinline__ Range make_range(const ChunkArgs& a) {
+  Range r;
+  r.kv_len = a.kv_len;
+  r.kv_start = a.kv_start;
+  r.k8 = a.k8;
+  r.v8 = a.v8;
+  r.m = a.m;
+  r.l = a.l;
+  r.o = a.o;
+  r.fresh = false;
+  if (a.split_keys > 0) {
+    const int64_t off = static_cast<int64_t>(blockIdx.y) * a.split_keys;
+    const int64_t rows = static_cast<int64_t>(a.bh) * a.n_q;
+    r.kv_len = i64min(a.split_keys, a.kv_len - off);
+    r.kv_start = a.kv_start + off;
+    r.k8 = a.k8 + off * kRowBytes;
+    r.v8 = a.v8 + off * kRowBytes;
+    r.m = a.part_m + blockIdx.y * rows;
+    r.l = a.part_l + blockIdx.y * rows;
+    r.o = a.part_o + blockIdx.y * rows * kHeadDim;
+    r.fresh = true;
+  }
+  return r;
+}
+
 // Per-CTA work description.
 struct Unit {
   int64_t bh, b, h, r0;   // (batch*heads index), first row of tile A
@@ -214,7 +251,7 @@ struct Unit {
   int T_all;              // max over tiles
 };
 
-__device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
+__device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
   const int64_t idx = blockIdx.x;
   u.bh = idx / a.n_qtiles;   // n_qtiles counts 256-row units here
@@ -229,8 +266,8 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
     u.T[x] = 0;
     if (rx < a.n_q) {
       const int64_t r_last = i64min(rx + BM - 1, a.n_q - 1);
-      int64_t n_vis = a.kv_len;
-      if (a.causal) n_vis = i64min(n_vis, a.q_pos0 + r_last - a.kv_start + 1);
+      int64_t n_vis = kr.kv_len;
+      if (a.causal) n_vis = i64min(n_vis, a.q_pos0 + r_last - kr.kv_start + 1);
       u.T[x] = n_vis > 0 ? static_cast<int>((n_vis + BN - 1) / BN) : 0;
     }
     u.T_all = max(u.T_all, u.T[x]);
@@ -241,8 +278,8 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
 // ------------------------------------------------------------------ roles --
 
 __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const ChunkArgs& a,
-                                              const Unit& u, uint8_t* smem, uint32_t sbase,
-                                              Ctl* ctl) {
+                                              const Range& kr, const Unit& u, uint8_t* smem,
+                                              uint32_t sbase, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;   // cycles
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
@@ -266,14 +303,14 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
 #pragma unroll
   for (int s = 0; s < NR; ++s) last_bulk[s] = -1;
 
-  const uint8_t* kp = a.k8 + u.bh * a.plane_stride;
-  const uint8_t* vp = a.v8 + u.bh * a.plane_stride;
+  const uint8_t* kp = kr.k8 + u.bh * a.plane_stride;
+  const uint8_t* vp = kr.v8 + u.bh * a.plane_stride;
   for (int t = 0; t < u.T_all; ++t) {
     const int sr = t % NR;
     if (!wait_bar(bar(B_RAWEMPTY + sr), ((t / NR) & 1) ^ 1, ctl, budget, R_PRODUCER, true))
       break;
     const int64_t k0 = static_cast<int64_t>(t) * BN;
-    const int n = static_cast<int>(i64min(BN, a.kv_len - k0));
+    const int n = static_cast<int>(i64min(BN, kr.kv_len - k0));
     const uint32_t bytes = static_cast<uint32_t>(n) * kRowBytes;
     const uint32_t dk = sbase + OFF_RAW + sr * 2 * RAWB;
     if ((bytes & 15u) == 0u) {
@@ -346,8 +383,8 @@ __device__ __forceinline__ void dequant_block(const uint32_t (&w)[9], int blk, u
   }
 }
 
-__device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, uint8_t* smem,
-                                             uint32_t sbase, Ctl* ctl) {
+__device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Range& kr, const Unit& u,
+                                             uint8_t* smem, uint32_t sbase, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;   // cycles
   const int k = threadIdx.x - 256;   // key row of the tile
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
@@ -358,7 +395,7 @@ __device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Unit& u, 
     if (!wait_bar(bar(B_RAWFULL + sr), (t / NR) & 1, ctl, budget, R_DEQUANT, true)) break;
     if (!wait_bar(bar(B_DEQEMPTY + sd), ((t / ND) & 1) ^ 1, ctl, budget, R_DEQUANT, true))
       break;
-    const int n_valid = static_cast<int>(i64min(BN, a.kv_len - static_cast<int64_t>(t) * BN));
+    const int n_valid = static_cast<int>(i64min(BN, kr.kv_len - static_cast<int64_t>(t) * BN));
     uint8_t* dq = smem + OFF_DEQ + sd * DEQ_BYTES + row_off;
     if (k < n_valid) {
 #pragma unroll 1
@@ -502,7 +539,7 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
   wait_bar(bar(B_DRAIN), 0, ctl, budget, R_DRAIN, false);
 }
 
-__device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, int x,
+__device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr, const Unit& u, int x,
                                              uint32_t sbase, uint32_t tmem, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;   // cycles
   const int row = threadIdx.x & 127;       // TMEM lane
@@ -514,21 +551,21 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
 
   const int64_t rg = u.r0 + x * BM + row;
   const int64_t pos = a.q_pos0 + rg;
-  const bool active = rg < a.n_q && (!a.causal || pos >= a.kv_start);
+  const bool active = rg < a.n_q && (!a.causal || pos >= kr.kv_start);
   const int64_t sidx = u.bh * a.n_q + rg;
   const uint32_t t_s = tmem + lane_off + T_S + 128u * x;
   const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
 
   float m_run = -INFINITY, l_run = 0.0f;
-  if (active) {
-    m_run = a.m[sidx];
-    l_run = a.l[sidx];
+  if (active && !kr.fresh) {
+    m_run = kr.m[sidx];
+    l_run = kr.l[sidx];
   }
   {
     // the O row enters TMEM as the high half; the residual half starts at 0
     uint32_t oh[64];
-    if (active) {
-      const float4* src = reinterpret_cast<const float4*>(a.o + sidx * kHeadDim);
+    if (active && !kr.fresh) {
+      const float4* src = reinterpret_cast<const float4*>(kr.o + sidx * kHeadDim);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float4 p = src[i];
@@ -571,10 +608,10 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
     tmem_wait_ld_at<96>(s);
 
     const int64_t k0 = static_cast<int64_t>(t) * BN;
-    const bool need_mask = (k0 + BN > a.kv_len) || (a.causal && a.kv_start + k0 + BN - 1 > q_first);
+    const bool need_mask = (k0 + BN > kr.kv_len) || (a.causal && kr.kv_start + k0 + BN - 1 > q_first);
     if (__builtin_expect(need_mask, 0)) {
-      int64_t lim = a.kv_len - 1 - k0;
-      if (a.causal) lim = i64min(lim, pos - a.kv_start - k0);
+      int64_t lim = kr.kv_len - 1 - k0;
+      if (a.causal) lim = i64min(lim, pos - kr.kv_start - k0);
       const int li = static_cast<int>(i64max(-1, i64min(lim, BN - 1)));
 #pragma unroll
       for (int j = 0; j < 128; ++j)
@@ -656,8 +693,8 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
     if (wait_bar(bar(B_ODONE + x), 0, ctl, budget, R_SOFTMAX, true)) {
       tc_fence_after();
       if (active) {
-        a.m[sidx] = m_run;
-        a.l[sidx] = l_run;
+        kr.m[sidx] = m_run;
+        kr.l[sidx] = l_run;
       }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -667,7 +704,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Unit& u, 
         tmem_wait_ld(oh);
         tmem_wait_ld(ol);
         if (active) {
-          float4* dst = reinterpret_cast<float4*>(a.o + sidx * kHeadDim) + 8 * half;
+          float4* dst = reinterpret_cast<float4*>(kr.o + sidx * kHeadDim) + 8 * half;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float v[4];
@@ -692,7 +729,8 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   const int warp = threadIdx.x >> 5;
   const int wg = warp >> 2;
 
-  const Unit u = make_unit(a);
+  const Range kr = make_range(a);
+  const Unit u = make_unit(a, kr);
   if (u.T_all == 0) return;   // uniform over the CTA: no visible key for these rows
 
   if (threadIdx.x == 0) {
@@ -719,13 +757,13 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   // fragments; the other warpgroups need far fewer registers.
   if (wg < 2) {
     reg_alloc<kRegSoftmax>();
-    softmax_role(a, u, wg, sbase, tmem, ctl);
+    softmax_role(a, kr, u, wg, sbase, tmem, ctl);
   } else {
     reg_dealloc<kRegOther>();
     if (wg == 2) {
-      dequant_role(a, u, smem, sbase, ctl);
+      dequant_role(a, kr, u, smem, sbase, ctl);
     } else if (warp == 12) {
-      producer_role(&qmap, a, u, smem, sbase, ctl);
+      producer_role(&qmap, a, kr, u, smem, sbase, ctl);
     } else if (warp == 13) {
       mma_role(a, u, sbase, tmem, ctl);
     }
@@ -758,7 +796,8 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
   const int64_t blocks = static_cast<int64_t>(units.n_qtiles) * units.bh;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  chunk_step_kernel<<<static_cast<unsigned>(blocks), kThreads, SMEM_BYTES, stream>>>(qmap, units);
+  const unsigned gy = args.split_keys > 0 ? static_cast<unsigned>(args.n_splits) : 1u;
+  chunk_step_kernel<<<dim3(static_cast<unsigned>(blocks), gy), kThreads, SMEM_BYTES, stream>>>(qmap, units);
   return cudaGetLastError();
 }
 

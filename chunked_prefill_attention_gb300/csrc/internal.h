@@ -43,11 +43,23 @@ struct ChunkArgs {
   int32_t causal;
   int32_t inject;         // test hook: 1 = first block skips its query-tile load
   uint64_t timeout_ns;    // budget of every device-side wait
+  // Split form (split_keys > 0): block row y of the grid folds keys
+  // [y*split_keys, min((y+1)*split_keys, kv_len)) of the chunk into an empty
+  // partial state at part_m/part_l/part_o + y * (bh*n_q) rows; the partials
+  // are merged into m/l/o by launch_split_merge.
+  int64_t split_keys;
+  int32_t n_splits;
+  float* part_m;
+  float* part_l;
+  float* part_o;
 };
 
 // The tensor map must describe Q as fp16 {H*64, n_q, B} with a {64, 128, 1}
 // box and 128-byte swizzle.
 cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
+
+// Merge the n_splits partial states of a split chunk step into (m, l, o).
+cudaError_t launch_split_merge(const ChunkArgs& args, cudaStream_t stream);
 
 // Status word of the current device (bit 0: a device-side wait ran out).
 cudaError_t read_device_status(cudaStream_t stream, uint32_t* status, bool clear);

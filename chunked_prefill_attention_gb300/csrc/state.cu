@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kThreads = 256;
 
+__host__ __device__ __forceinline__ int64_t i64min_host(int64_t a, int64_t b) { return a < b ? a : b; }
+
 __global__ void __launch_bounds__(kThreads)
 state_init_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
                   int64_t rows) {
@@ -62,6 +64,63 @@ finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4
   }
 }
 
+// Merge of the split partial states into the state, one (b, h, row) per 8
+// threads (8 channels each).  It is the chunk recurrence applied with a
+// partial's (m_s, l_s, O_s) in place of a chunk's row max, weight sum and
+// weighted values:  m' = max(m, m_s...),  l' = l e^(m - m') + sum_s l_s e^(m_s - m'),
+// O' = O e^(m - m') + sum_s O_s e^(m_s - m').  A partial is read only when its
+// key range holds a key the row can see (the chunk-step kernel writes exactly
+// those rows).
+__global__ void __launch_bounds__(kThreads)
+split_merge_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
+                   const float* __restrict__ pm, const float* __restrict__ pl,
+                   const float4* __restrict__ po, int64_t rows, int64_t n_q, int64_t q_pos0,
+                   int64_t kv_start, int64_t split_keys, int32_t n_splits, int32_t causal) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * 8;
+       g += stride) {
+    const int64_t row = g >> 3;   // (b*H + h)*n_q + r
+    const int part = static_cast<int>(g & 7);
+    const int64_t pos = q_pos0 + row % n_q;
+    // splits whose first key the row can see (all of them without the mask)
+    int ns = n_splits;
+    if (causal) {
+      const int64_t vis = pos - kv_start;   // keys 0 .. vis of the chunk are visible
+      ns = vis < 0 ? 0 : static_cast<int>(i64min_host(n_splits, vis / split_keys + 1));
+    }
+    if (ns == 0) continue;
+    const float m0 = m[row];   // every read of this row's m and l happens here
+    const float l0 = l[row];
+    float mx = m0;
+    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, pm[s * rows + row]);
+    if (mx == -INFINITY) continue;
+    const float f = (m0 == -INFINITY) ? 0.0f : expf(m0 - mx);
+    float lv = l0 * f;
+    float4 a = o[row * 16 + 2 * part], c = o[row * 16 + 2 * part + 1];
+    float y[8] = {a.x * f, a.y * f, a.z * f, a.w * f, c.x * f, c.y * f, c.z * f, c.w * f};
+    for (int s = 0; s < ns; ++s) {
+      const float ms = pm[s * rows + row];
+      if (ms == -INFINITY) continue;
+      const float w = expf(ms - mx);
+      lv = fmaf(pl[s * rows + row], w, lv);
+      const float4 pa = po[(s * rows + row) * 16 + 2 * part];
+      const float4 pc = po[(s * rows + row) * 16 + 2 * part + 1];
+      y[0] = fmaf(pa.x, w, y[0]); y[1] = fmaf(pa.y, w, y[1]);
+      y[2] = fmaf(pa.z, w, y[2]); y[3] = fmaf(pa.w, w, y[3]);
+      y[4] = fmaf(pc.x, w, y[4]); y[5] = fmaf(pc.y, w, y[5]);
+      y[6] = fmaf(pc.z, w, y[6]); y[7] = fmaf(pc.w, w, y[7]);
+    }
+    o[row * 16 + 2 * part] = make_float4(y[0], y[1], y[2], y[3]);
+    o[row * 16 + 2 * part + 1] = make_float4(y[4], y[5], y[6], y[7]);
+    // the row's eight lanes took the same path; all have read m and l by now
+    __syncwarp(0xFFu << ((threadIdx.x & 31) & ~7));
+    if (part == 0) {
+      m[row] = mx;
+      l[row] = lv;
+    }
+  }
+}
+
 int grid_for(int64_t work) {
   int64_t blocks = (work + kThreads - 1) / kThreads;
   const int64_t cap = 152 * 16;   // a few waves of resident blocks; grid-stride beyond
@@ -85,6 +144,16 @@ cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t b
   if (rows <= 0) return cudaSuccess;
   finalize_kernel<<<grid_for(rows * 8), kThreads, 0, stream>>>(
       l, reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_merge(const ChunkArgs& a, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(a.bh) * a.n_q;
+  if (rows <= 0 || a.n_splits <= 0) return cudaSuccess;
+  split_merge_kernel<<<grid_for(rows * 8), kThreads, 0, stream>>>(
+      a.m, a.l, reinterpret_cast<float4*>(a.o), a.part_m, a.part_l,
+      reinterpret_cast<const float4*>(a.part_o), rows, a.n_q, a.q_pos0, a.kv_start, a.split_keys,
+      a.n_splits, a.causal);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,9 @@ SIGNATURES = {
     "attn_state_init": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
     "attn_chunk_step": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32,
                                        _I64, _I32, _F, _I32, _P]),
+    "attn_chunk_step_split": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
+                                             _I32, _I64, _I32, _F, _I32, _I64, _P, _I64, _P]),
+    "q8a_split_workspace_floats": (_I64, [_I64, _I32, _I64, _I64, _I64]),
     "attn_finalize": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
     "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
     "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),
@@ -135,6 +138,36 @@ def attn_chunk_step(q, k8, v8, kv_start, kv_len, state, q_pos0=0, scale=None, ca
     _check(lib.attn_chunk_step(_ptr(q), q_pos0, kp, vp, stride, kv_start, kv_len, _ptr(state.m),
                                _ptr(state.l), _ptr(state.o), B, H, n_q, D, scale, int(bool(causal)),
                                _stream(q)))
+    return state
+
+
+def split_workspace_floats(batch, heads, n_q, kv_len, split_keys):
+    n = int(load().q8a_split_workspace_floats(batch, heads, n_q, kv_len, split_keys))
+    if n < 0:
+        raise Q8AttnError(Q8A_ERR_INVALID_ARG, "invalid sizes for the split workspace")
+    return n
+
+
+def attn_chunk_step_split(q, k8, v8, kv_start, kv_len, state, split_keys, workspace=None, q_pos0=0,
+                          scale=None, causal=True, stride=None, k_offset_bytes=0):
+    """attn_chunk_step with the chunk's keys folded in parallel ranges of
+    `split_keys` keys and merged.  `workspace`: fp32 CUDA tensor of at least
+    split_workspace_floats(...) elements (allocated here when None)."""
+    B, n_q, H, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stride is None:
+        stride = k8.shape[-1]
+    need = split_workspace_floats(B, H, n_q, kv_len, split_keys)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.float32, device=q.device)
+    lib = load()
+    kp = ctypes.c_void_p(k8.data_ptr() + k_offset_bytes)
+    vp = ctypes.c_void_p(v8.data_ptr() + k_offset_bytes)
+    _check(lib.attn_chunk_step_split(_ptr(q), q_pos0, kp, vp, stride, kv_start, kv_len,
+                                     _ptr(state.m), _ptr(state.l), _ptr(state.o), B, H, n_q, D,
+                                     scale, int(bool(causal)), split_keys, _ptr(workspace),
+                                     workspace.numel(), _stream(q)))
     return state
 
 

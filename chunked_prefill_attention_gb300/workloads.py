@@ -17,6 +17,13 @@ dimension 64 and a causal mask, computed chunk by chunk over the KV:
 The pages measure no public dataset; these draws stand in for the activations
 of a prefill pass.  Inputs are drawn with a torch generator on the device they
 are created on, in the fixed order Q, then K, then V.
+
+Mode B (speculative burst verification) has one workload of its own:
+
+  burst_m1m  64 candidate queries at positions M .. M+63 against an
+             M = 1,048,576-token context, 32 heads x 64, rectangular
+             full-context mask; Q ~ N(0,1) fp16, K, V ~ N(0,1) fp32 (seed 5);
+             the context's keys are folded in ranges of 8,192.
 """
 
 from dataclasses import dataclass
@@ -68,6 +75,47 @@ WORKLOADS = {
         Workload("m1m", 1, 1048576, 131072, 4),
     ]
 }
+
+
+@dataclass(frozen=True)
+class Burst:
+    name: str
+    context: int
+    queries: int
+    split_keys: int
+    seed: int
+    heads: int = HEADS
+    head_dim: int = HEAD_DIM
+
+    @property
+    def kv_bytes(self):
+        """Q8_0 K and V of the context: 2 * H * M * 68 bytes."""
+        return 2 * self.heads * self.context * 68
+
+    @property
+    def flops(self):
+        """4*D flops per (candidate, context key) pair."""
+        return 4 * self.head_dim * self.heads * self.queries * self.context
+
+    def describe(self):
+        return (f"{self.name}: {self.queries} candidate queries after a {self.context}-token context, "
+                f"H={self.heads} D={self.head_dim}, rectangular mask, key ranges of "
+                f"{self.split_keys}, seed {self.seed}")
+
+
+BURSTS = {b.name: b for b in [Burst("burst_m1m", 1048576, 64, 8192, 5)]}
+
+
+def make_burst_inputs(b, device="cpu", context=None):
+    """Draw (Q fp16 [1, queries, H, D], K fp32 [1, M, H, D], V fp32), in that order."""
+    M = b.context if context is None else context
+    g = torch.Generator(device=device)
+    g.manual_seed(b.seed)
+    q = torch.randn((1, b.queries, b.heads, b.head_dim), generator=g, device=device,
+                    dtype=torch.float32).to(torch.float16)
+    k = torch.randn((1, M, b.heads, b.head_dim), generator=g, device=device, dtype=torch.float32)
+    v = torch.randn((1, M, b.heads, b.head_dim), generator=g, device=device, dtype=torch.float32)
+    return q, k, v
 
 
 def make_inputs(w, device="cpu", batch=None, tokens=None):

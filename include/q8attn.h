@@ -60,6 +60,7 @@ enum {
 };
 
 #define Q8A_ROW_BYTES 68 /* one 64-channel head row: two 34-byte Q8_0 blocks */
+#define Q8A_HEAD_DIM 64  /* the supported head dimension */
 
 /* ABI version of the loaded library (Q8A_ABI_VERSION). */
 uint32_t q8a_abi_version(void);
@@ -135,6 +136,39 @@ int attn_chunk_step(const void *q, int64_t q_pos0, const void *k_q8, const void 
                     float *m, float *l, float *o, int64_t batch, int32_t heads,
                     int64_t n_q, int32_t head_dim, float scale, int32_t causal,
                     void *stream);
+
+/*
+ * attn_chunk_step_split -- the same update as attn_chunk_step for query rows
+ * that are few against a long chunk, such as Mode B speculative burst
+ * verification ([STREAM §4]: K = 64 candidate queries against the whole
+ * context, rectangular full-context mask, bound by reading the KV cache once).
+ * The chunk's keys are cut into ranges of split_keys keys that are folded in
+ * parallel, each into an empty partial state (m_s, l_s, O_s) in `workspace`;
+ * a second kernel then folds the partials into (m, l, O) with the same
+ * recurrence ([STREAM §3] steps 3-6, with a partial's max, weight sum and
+ * weighted values in place of a chunk's).  The result equals attn_chunk_step's
+ * up to floating-point rounding.  Arguments as for attn_chunk_step, plus:
+ *   split_keys        keys per range, a positive multiple of 128.
+ *   workspace         caller-owned fp32 scratch, 16-byte aligned, of at least
+ *                     q8a_split_workspace_floats(batch, heads, n_q, kv_len,
+ *                     split_keys) floats; its contents are overwritten.  Calls
+ *                     sharing one workspace must be ordered on one stream.
+ *   workspace_floats  its size in floats.
+ * Two kernel launches on `stream`.  Errors: as attn_chunk_step; Q8A_ERR_INVALID_ARG
+ * also for a bad split_keys or a missing or too small workspace;
+ * Q8A_ERR_UNSUPPORTED beyond 65,535 key ranges.
+ */
+int attn_chunk_step_split(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,
+                          int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                          float *m, float *l, float *o, int64_t batch, int32_t heads,
+                          int64_t n_q, int32_t head_dim, float scale, int32_t causal,
+                          int64_t split_keys, float *workspace, int64_t workspace_floats,
+                          void *stream);
+
+/* Floats of workspace attn_chunk_step_split needs:
+ * ceil(kv_len / split_keys) * batch * heads * n_q * 66; -1 for invalid sizes. */
+int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
+                                   int64_t split_keys);
 
 /*
  * attn_finalize -- out_i = O_i / l_i after the last chunk [STREAM §3]; a row

@@ -108,6 +108,30 @@ def test_chunk_step_validation(lib):
     assert call(kv_start=128, n_q=128) == Q.Q8A_OK
 
 
+def test_split_step_validation(lib):
+    """attn_chunk_step_split rejects bad range sizes and workspaces before it
+    touches the device."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    s = P(0)
+    need = lib.q8a_split_workspace_floats(1, 2, 128, 1000, 256)
+    assert need == 4 * 1 * 2 * 128 * 66
+    assert lib.q8a_split_workspace_floats(1, 2, 128, 1000, 0) == -1
+    assert lib.q8a_split_workspace_floats(-1, 2, 128, 1000, 256) == -1
+
+    def call(split=256, ws=A16, ws_n=need, kv_len=1000, stride=68000, causal=0):
+        return lib.attn_chunk_step_split(A16, 0, A16, A16, stride, 0, kv_len, A16, A16, A16, 1, 2, 128,
+                                         64, 0.125, causal, split, ws, ws_n, s)
+
+    assert call(split=0) == Q.Q8A_ERR_INVALID_ARG
+    assert call(split=100) == Q.Q8A_ERR_INVALID_ARG
+    assert call(ws=P(0)) == Q.Q8A_ERR_INVALID_ARG
+    assert call(ws_n=need - 1) == Q.Q8A_ERR_INVALID_ARG
+    assert call(ws=P(0x100008)) == Q.Q8A_ERR_MISALIGNED
+    assert call(split=128, kv_len=128 * 70000, stride=68 * 128 * 70000,
+                ws_n=1 << 62) == Q.Q8A_ERR_UNSUPPORTED
+    assert call(kv_len=0, ws=P(0), ws_n=0) == Q.Q8A_OK
+
+
 def test_runtime_knobs_validation(lib):
     from chunked_prefill_attention_gb300 import q8attn as Q
     assert lib.q8a_set_wait_timeout_ns(10) == Q.Q8A_ERR_INVALID_ARG

@@ -1,0 +1,117 @@
+"""attn_chunk_step_split (the chunk's keys folded in parallel ranges, each into
+its own partial state, then merged) against the oracle: Mode B burst
+verification -- 64 candidate queries after the context, rectangular
+full-context attention ("Out-of-Core Flash Streaming & Speculative Decode (1M
+Context)", §4) -- and causal prefill with ragged ranges."""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.conftest import cuda_available
+from tests.parity import assert_device_clean, compare, gpu_bytes, oracle_out, seeded
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+
+def _kv(B, M, H, seed, scale=1.0):
+    k = seeded((B, M, H, 64), seed, "cuda", scale=scale)
+    v = seeded((B, M, H, 64), seed + 1, "cuda", scale=scale)
+    return k, v
+
+
+@pytest.mark.parametrize("M,H,split", [(4096, 4, 512), (3000, 2, 384), (700, 3, 128)])
+def test_burst_verification_rectangular(lib, M, H, split):
+    """64 candidate queries at positions M .. M+63 see every context key."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    q = seeded((1, 64, H, 64), M + 1, "cuda", torch.float16)
+    k, v = _kv(1, M, H, M + 2)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, 64, q.device)
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, st, split, q_pos0=M, causal=False)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want, wk8, wv8 = oracle_out(q, k, v, causal=False, q_pos0=M)
+    assert np.array_equal(gpu_bytes(k8, M), wk8) and np.array_equal(gpu_bytes(v8, M), wv8)
+    compare(out.cpu().numpy(), want, f"burst M{M} split{split}")
+
+
+@pytest.mark.parametrize("M,chunk,split", [(1000, 1000, 256), (1029, 512, 128), (2048, 2048, 1024)])
+def test_causal_prefill_split(lib, M, chunk, split):
+    """Causal prefill with every chunk split: later ranges are invisible to the
+    early rows of a chunk, whose partials the merge must skip."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    H = 3
+    q = seeded((1, M, H, 64), M + 11, "cuda", torch.float16)
+    k, v = _kv(1, M, H, M + 12)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, M, q.device)
+    for s0 in range(0, M, chunk):
+        Q.attn_chunk_step_split(q, k8, v8, s0, min(chunk, M - s0), st, split, k_offset_bytes=s0 * 68)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want, *_ = oracle_out(q, k, v)
+    compare(out.cpu().numpy(), want, f"causal split M{M} chunk{chunk} split{split}")
+
+
+def test_split_matches_unsplit(lib):
+    """Split and unsplit forms of the same update: the running max is exact in
+    both, so m is bit-identical; l agrees to fp32 rounding; the weights are
+    rounded to fp16 against each key range's own max before the merge, so the
+    outputs agree within the parity tolerance rather than bit for bit."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    M, H = 2304, 2
+    q = seeded((1, 64, H, 64), 41, "cuda", torch.float16)
+    k, v = _kv(1, M, H, 42, scale=1.5)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    a = Q.State(1, H, 64, q.device)
+    b = Q.State(1, H, 64, q.device)
+    Q.attn_chunk_step(q, k8, v8, 0, M, a, q_pos0=M, causal=False)
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, b, 256, q_pos0=M, causal=False)
+    assert_device_clean()
+    assert torch.equal(a.m, b.m)
+    assert torch.allclose(a.l, b.l, rtol=1e-5, atol=0)
+    oa, ob = Q.attn_finalize(a).float(), Q.attn_finalize(b).float()
+    assert torch.max(torch.abs(oa - ob)).item() <= 2e-3
+    want, *_ = oracle_out(q, k, v, causal=False, q_pos0=M)
+    compare(ob.cpu().numpy(), want, "split")
+
+
+def test_split_continues_a_state(lib):
+    """An unsplit chunk, then a split one, into the same state."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    M, H = 1536, 2
+    q = seeded((1, M, H, 64), 51, "cuda", torch.float16)
+    k, v = _kv(1, M, H, 52)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, M, q.device)
+    Q.attn_chunk_step(q, k8, v8, 0, 512, st)
+    ws = torch.empty(Q.split_workspace_floats(1, H, M, 1024, 256), dtype=torch.float32, device="cuda")
+    Q.attn_chunk_step_split(q, k8, v8, 512, 1024, st, 256, workspace=ws, k_offset_bytes=512 * 68)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want, *_ = oracle_out(q, k, v)
+    compare(out.cpu().numpy(), want, "unsplit then split")
+
+
+def test_burst_verification_long_context(lib):
+    """64 candidates against a 131,072-token, 32-head Q8_0 context, in 64
+    key ranges of 2,048 keys."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    from oracle import runner as oracle_runner
+    M, H = 131072, 32
+    q = seeded((1, 64, H, 64), 61, "cuda", torch.float16)
+    k, v = _kv(1, M, H, 62)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, 64, q.device)
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, st, 2048, q_pos0=M, causal=False)
+    out = Q.attn_finalize(st).cpu().numpy()
+    assert_device_clean()
+    wk8 = oracle_runner.quantize_kv(k.cpu().numpy())
+    assert np.array_equal(gpu_bytes(k8, M), wk8)
+    del k
+    wv8 = oracle_runner.quantize_kv(v.cpu().numpy())
+    assert np.array_equal(gpu_bytes(v8, M), wv8)
+    del v
+    want = oracle_runner.attention(q.cpu().numpy(), wk8, wv8, 0.125, causal=False, q_pos0=M)
+    compare(out, want, "burst 131072")
