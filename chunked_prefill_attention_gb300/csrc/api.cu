@@ -261,6 +261,71 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
   return ok();
 }
 
+}  // extern "C"
+
+// ---- allocation-free split step ----------------------------------------------
+// Scratch for attn_chunk_step_split_static: the partial states live in this
+// fixed array, which every GPU that loads the library holds until the process
+// exits.  In host code the symbol is only a stand-in; its device address is
+// fetched once per device (with that device current) and handed to the
+// kernels like any workspace.
+namespace {
+
+constexpr int64_t kStaticSplitFloats = 8ll * 1024 * 1024;   // 32 MiB
+__device__ __align__(256) float g_static_split_scratch[kStaticSplitFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+float* g_static_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (looked up on first use).
+int static_scratch(const char* fn, float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: device ordinal %d beyond %d", fn, dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_split_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return Q8A_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t q8a_static_split_scratch_floats(void) { return kStaticSplitFloats; }
+
+int attn_chunk_step_split_static(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                                 int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                                 float* m, float* l, float* o, int64_t batch, int32_t heads,
+                                 int64_t n_q, int32_t head_dim, float scale, int32_t causal,
+                                 int64_t split_keys, void* stream) {
+  const char* fn = "attn_chunk_step_split_static";
+  if (split_keys <= 0 || split_keys % 128 != 0)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
+                fn, (long long)split_keys);
+  float* ws = nullptr;
+  if (batch > 0 && heads > 0 && n_q > 0 && kv_len > 0) {
+    const int64_t need = q8a_split_workspace_floats(batch, heads, n_q, kv_len, split_keys);
+    if (need > kStaticSplitFloats)
+      return fail(Q8A_ERR_INVALID_ARG,
+                  "%s: the partial states need %lld floats, more than the %lld of the static "
+                  "scratch; use larger key ranges or attn_chunk_step_split",
+                  fn, (long long)need, (long long)kStaticSplitFloats);
+    if (int rc = static_scratch(fn, &ws)) return rc;
+  }
+  return attn_chunk_step_split(q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start, kv_len, m, l,
+                               o, batch, heads, n_q, head_dim, scale, causal, split_keys, ws,
+                               kStaticSplitFloats, stream);
+}
+
 int attn_finalize(const float* l, const float* o, void* out, int64_t batch, int32_t heads,
                   int64_t n_q, int32_t head_dim, void* stream) {
   const char* fn = "attn_finalize";

@@ -39,6 +39,9 @@ SIGNATURES = {
     "attn_chunk_step_split": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
                                              _I32, _I64, _I32, _F, _I32, _I64, _P, _I64, _P]),
     "q8a_split_workspace_floats": (_I64, [_I64, _I32, _I64, _I64, _I64]),
+    "attn_chunk_step_split_static": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P,
+                                                    _I64, _I32, _I64, _I32, _F, _I32, _I64, _P]),
+    "q8a_static_split_scratch_floats": (_I64, []),
     "attn_finalize": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
     "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
     "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),

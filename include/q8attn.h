@@ -171,6 +171,37 @@ int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, in
                                    int64_t split_keys);
 
 /*
+ * attn_chunk_step_split_static -- attn_chunk_step_split for callers that
+ * cannot allocate device memory when they make the call: for instance code
+ * embedded in a host framework that owns the device allocator and forbids
+ * other allocations, or a latency-critical loop that cannot afford the
+ * implicit device synchronisation of cudaMalloc / cudaFree.  It allocates
+ * nothing: the partial states live in a fixed scratch array inside the
+ * library (q8a_static_split_scratch_floats() floats = 32 MiB on every GPU that
+ * loads the library, held until the process exits).  The source pages have no
+ * counterpart: this is an interface convenience, not part of the method.
+ *   Arguments, result and errors: as attn_chunk_step_split without the
+ *   workspace.  A call whose partial states would need more floats than the
+ *   scratch holds (q8a_split_workspace_floats(...) > the scratch size) is
+ *   rejected with Q8A_ERR_INVALID_ARG before anything is launched; use larger
+ *   key ranges or attn_chunk_step_split with a workspace of your own.
+ *   The first call on a device looks up the scratch's device address on that
+ *   (current) device; make that first call before any stream capture.
+ *   Every call on a device shares the one scratch array, which keeps the last
+ *   call's contents; each call writes every partial it later reads, so no
+ *   clearing is needed, but calls whose kernels can overlap on the GPU (other
+ *   streams, other host threads) race on it: order them on one stream.
+ */
+int attn_chunk_step_split_static(const void *q, int64_t q_pos0, const void *k_q8,
+                                 const void *v_q8, int64_t kv_plane_stride_bytes,
+                                 int64_t kv_start, int64_t kv_len, float *m, float *l, float *o,
+                                 int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
+                                 float scale, int32_t causal, int64_t split_keys, void *stream);
+
+/* Size of the static scratch of attn_chunk_step_split_static, in floats. */
+int64_t q8a_static_split_scratch_floats(void);
+
+/*
  * attn_finalize -- out_i = O_i / l_i after the last chunk [STREAM §3]; a row
  * with l_i == 0 (it saw no key) gives 0.  out is fp16 (round to nearest even),
  * [B][n_q][H][64], 16-byte aligned; l 4-byte aligned; o 16-byte aligned.
