@@ -258,13 +258,11 @@ def run_ours(args):
         kh = k.cpu().pin_memory()
         vh = v.cpu().pin_memory()
         oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        bufs = Q.PipelineBuffers(B, M, H, dev)
 
         def e2e_step():
-            q.copy_(qh, non_blocking=True)
-            k.copy_(kh, non_blocking=True)
-            v.copy_(vh, non_blocking=True)
-            step()
-            oh.copy_(out, non_blocking=True)
+            # attn_prefill_pipelined: K/V chunk copies overlap quantise + chunk steps
+            Q.attn_prefill_pipelined(qh, kh, vh, oh, w.chunk, bufs)
 
         e2e_step()
         torch.cuda.synchronize()

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libq8attn.so")
-SOURCES = ["api.cu", "quantize.cu", "state.cu", "chunk_step.cu"]
+SOURCES = ["api.cu", "quantize.cu", "state.cu", "chunk_step.cu", "pipeline.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

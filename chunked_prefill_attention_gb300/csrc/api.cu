@@ -55,6 +55,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+int q8a::set_error(int code, const char* fn, const char* msg) {
+  return fail(code, "%s: %s", fn, msg);
+}
+
+namespace {
+
 int check_common(int64_t batch, int32_t heads, int32_t head_dim, const char* fn) {
   if (batch < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: batch must be >= 0 (got %lld)", fn, (long long)batch);
   if (heads <= 0) return fail(Q8A_ERR_INVALID_ARG, "%s: heads must be > 0 (got %d)", fn, heads);

@@ -58,6 +58,9 @@ struct ChunkArgs {
 // box and 128-byte swizzle.
 cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
 
+// Record `msg` as the calling thread's last error (q8a_last_error) and return code.
+int set_error(int code, const char* fn, const char* msg);
+
 // Merge the n_splits partial states of a split chunk step into (m, l, o).
 cudaError_t launch_split_merge(const ChunkArgs& args, cudaStream_t stream);
 

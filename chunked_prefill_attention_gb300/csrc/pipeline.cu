@@ -1,0 +1,100 @@
+// pipeline.cu -- the whole prefill from host buffers, with the host-to-device
+// copy of each KV chunk overlapped with the device work on the chunks before
+// it.
+//
+// This is the GB300 form of the pages' out-of-core streaming ("Out-of-Core
+// Flash Streaming & Speculative Decode (1M Context)", §2: while the GPU folds
+// chunk c into the persistent state, the next chunk is already being read into
+// a second buffer).  Here the source is pinned host memory instead of flash,
+// the copies run on a copy stream, and each chunk's Q8_0 quantisation and
+// chunk step wait on that chunk's copy through an event.  Host code only: every
+// step of the computation is one of the library's kernels.
+
+#include <cstdio>
+
+#include "../../include/q8attn.h"
+#include "internal.h"
+
+namespace {
+
+constexpr const char* kFn = "attn_prefill_pipelined";
+
+int cuda_err(cudaError_t e, const char* what) {
+  char msg[256];
+  std::snprintf(msg, sizeof(msg), "%s: %s", what, cudaGetErrorName(e));
+  return q8a::set_error(Q8A_ERR_CUDA, kFn, msg);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_prefill_pipelined(const void* q_host, const float* k_host, const float* v_host,
+                           void* out_host, int64_t batch, int32_t heads, int64_t n_tokens,
+                           int32_t head_dim, int64_t chunk, float scale, int32_t causal,
+                           void* q_dev, float* k_dev, float* v_dev, void* k8, void* v8,
+                           int64_t plane_stride_bytes, float* m, float* l, float* o, void* out_dev,
+                           void* compute_stream, void* copy_stream) {
+  if (batch < 0 || heads <= 0 || n_tokens < 0 || head_dim != Q8A_HEAD_DIM || chunk <= 0 ||
+      chunk % 4 != 0)
+    return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn,
+                          "sizes must be >= 0, heads > 0, head_dim 64 and chunk a positive "
+                          "multiple of 4");
+  if (batch == 0 || n_tokens == 0) return Q8A_OK;
+  if (!q_host || !k_host || !v_host || !out_host || !q_dev || !k_dev || !v_dev || !k8 || !v8 ||
+      !m || !l || !o || !out_dev)
+    return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn, "null pointer");
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const int64_t row_floats = static_cast<int64_t>(heads) * Q8A_HEAD_DIM;   // one token, all heads
+  const size_t q_bytes = static_cast<size_t>(batch * n_tokens * row_floats) * 2;
+  const size_t out_bytes = q_bytes;
+
+  cudaEvent_t ev = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_err(e, "cudaEventCreateWithFlags");
+  int rc = Q8A_OK;
+  auto bail = [&](int code) {
+    cudaEventDestroy(ev);   // released once the recorded work is done
+    return code;
+  };
+  // Earlier work on the compute stream may still read the device buffers that
+  // the copies below overwrite: the copy stream starts after it.
+  if ((e = cudaEventRecord(ev, cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+  if ((e = cudaStreamWaitEvent(xs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
+  if ((e = cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+    return bail(cuda_err(e, "copy of Q"));
+  if ((rc = attn_state_init(m, l, o, batch, heads, n_tokens, head_dim, cs)) != Q8A_OK) return bail(rc);
+
+  for (int64_t s0 = 0; s0 < n_tokens; s0 += chunk) {
+    const int64_t n = (n_tokens - s0 < chunk) ? n_tokens - s0 : chunk;
+    const size_t bytes = static_cast<size_t>(n * row_floats) * sizeof(float);
+    for (int64_t b = 0; b < batch; ++b) {
+      const int64_t off = (b * n_tokens + s0) * row_floats;
+      if ((e = cudaMemcpyAsync(k_dev + off, k_host + off, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(v_dev + off, v_host + off, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+        return bail(cuda_err(e, "copy of a K/V chunk"));
+    }
+    // the chunk (and, before it on the copy stream, Q) is on the device once ev fires
+    if ((e = cudaEventRecord(ev, xs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+    if ((e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
+    for (int64_t b = 0; b < batch; ++b) {
+      const int64_t off = (b * n_tokens + s0) * row_floats;
+      uint8_t* kq = static_cast<uint8_t*>(k8) + b * heads * plane_stride_bytes + s0 * Q8A_ROW_BYTES;
+      uint8_t* vq = static_cast<uint8_t*>(v8) + b * heads * plane_stride_bytes + s0 * Q8A_ROW_BYTES;
+      if ((rc = q8kv_quantize(k_dev + off, kq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK ||
+          (rc = q8kv_quantize(v_dev + off, vq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK)
+        return bail(rc);
+    }
+    if ((rc = attn_chunk_step(q_dev, 0, static_cast<const uint8_t*>(k8) + s0 * Q8A_ROW_BYTES,
+                              static_cast<const uint8_t*>(v8) + s0 * Q8A_ROW_BYTES, plane_stride_bytes,
+                              s0, n, m, l, o, batch, heads, n_tokens, head_dim, scale, causal, cs)) != Q8A_OK)
+      return bail(rc);
+  }
+  if ((rc = attn_finalize(l, o, out_dev, batch, heads, n_tokens, head_dim, cs)) != Q8A_OK) return bail(rc);
+  if ((e = cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
+    return bail(cuda_err(e, "copy of the output"));
+  return bail(Q8A_OK);
+}
+
+}  // extern "C"

@@ -43,6 +43,8 @@ SIGNATURES = {
                                                     _I64, _I32, _I64, _I32, _F, _I32, _I64, _P]),
     "q8a_static_split_scratch_floats": (_I64, []),
     "attn_finalize": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
+    "attn_prefill_pipelined": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, _I64, _I32, _I64, _F, _I32,
+                                              _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
     "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),
     "q8a_test_inject": (ctypes.c_int, [_I32]),
@@ -200,6 +202,38 @@ def prefill_attention(q, k, v, chunk, scale=None, causal=True, k8=None, v8=None,
                         k_offset_bytes=s0 * ROW_BYTES)
     out = attn_finalize(state, out)
     return out, k8, v8
+
+
+class PipelineBuffers:
+    """Device buffers of attn_prefill_pipelined for one problem size."""
+
+    def __init__(self, batch, n_tokens, heads, device):
+        shape = (batch, n_tokens, heads, HEAD_DIM)
+        self.q = torch.empty(shape, dtype=torch.float16, device=device)
+        self.k = torch.empty(shape, dtype=torch.float32, device=device)
+        self.v = torch.empty(shape, dtype=torch.float32, device=device)
+        self.out = torch.empty(shape, dtype=torch.float16, device=device)
+        self.stride = plane_stride(n_tokens)
+        self.k8 = torch.empty((batch, heads, self.stride), dtype=torch.uint8, device=device)
+        self.v8 = torch.empty((batch, heads, self.stride), dtype=torch.uint8, device=device)
+        self.state = State(batch, heads, n_tokens, device, init=False)
+        self.copy_stream = torch.cuda.Stream(device=device)
+
+
+def attn_prefill_pipelined(q_host, k_host, v_host, out_host, chunk, bufs, scale=None, causal=True):
+    """The whole prefill from host tensors (page-locked for overlap): K/V chunk
+    copies on bufs.copy_stream overlap quantise + chunk step on the current
+    stream; the output lands in out_host once the current stream drains."""
+    B, M, H, D = q_host.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = bufs.state
+    _check(load().attn_prefill_pipelined(
+        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), B, H, M, D, chunk, scale,
+        int(bool(causal)), _ptr(bufs.q), _ptr(bufs.k), _ptr(bufs.v), _ptr(bufs.k8), _ptr(bufs.v8),
+        bufs.stride, _ptr(st.m), _ptr(st.l), _ptr(st.o), _ptr(bufs.out), _stream(bufs.q),
+        ctypes.c_void_p(bufs.copy_stream.cuda_stream)))
+    return out_host
 
 
 def device_status(clear=True, stream=None):

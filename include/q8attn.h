@@ -8,8 +8,9 @@
  *            Barrier-Free FlashAttention & Dynamic Q8_0 KV Cache", part 2
  *            "Dynamic Q8_0 KV Cache Compression".
  *   [STREAM] "Out-of-Core Flash Streaming & Speculative Decode (1M Context)",
- *            §3 "Chunked FlashAttention: Exact Mathematical Derivation" and
- *            §4 "Mode A vs. Mode B Execution Modes".
+ *            §2 (the double-buffered streaming of KV chunks), §3 "Chunked
+ *            FlashAttention: Exact Mathematical Derivation" and §4 "Mode A vs.
+ *            Mode B Execution Modes".
  *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
@@ -208,6 +209,40 @@ int64_t q8a_static_split_scratch_floats(void);
  */
 int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int32_t heads,
                   int64_t n_q, int32_t head_dim, void *stream);
+
+/*
+ * attn_prefill_pipelined -- the whole prefill from host buffers ([STREAM §2]:
+ * the next KV chunk is read while the current one is folded into the state):
+ * Q is copied to the device, then for each chunk of `chunk` tokens its K and V
+ * are copied on `copy_stream` while `compute_stream` quantises and folds the
+ * chunks before it (q8kv_quantize on the chunk's tokens, attn_chunk_step with
+ * kv_start = the chunk's first token, q_pos0 = 0); finally attn_finalize and
+ * the copy of the output back to the host.  The result is bit-identical to
+ * quantising the whole K and V and folding the same chunks in order.
+ *   q_host, out_host   fp16 [B][n_tokens][H][64] in host memory;
+ *   k_host, v_host     fp32 [B][n_tokens][H][64] in host memory;
+ *                      page-locked host memory lets the copies overlap the
+ *                      device work (pageable memory works, without overlap).
+ *   q_dev, k_dev, v_dev, out_dev  device buffers of the same layouts and sizes;
+ *   k8, v8, plane_stride_bytes    the Q8_0 planes (as for q8kv_quantize);
+ *   m, l, o            the state (as for attn_state_init; initialised here);
+ *   chunk              tokens per chunk, a positive multiple of 4;
+ *   compute_stream, copy_stream   two streams (the same stream is allowed and
+ *                      then nothing overlaps).  Everything is enqueued
+ *                      asynchronously; the copy stream first waits for the
+ *                      work already on the compute stream, so back-to-back calls
+ *                      on the same buffers are ordered.  The output is on the
+ *                      host once compute_stream has drained.
+ * The call creates and releases one CUDA event; it allocates no memory.
+ * Errors: Q8A_ERR_INVALID_ARG (sizes, null pointers), those of the calls above,
+ * Q8A_ERR_CUDA (a copy, event or stream call failed).
+ */
+int attn_prefill_pipelined(const void *q_host, const float *k_host, const float *v_host,
+                           void *out_host, int64_t batch, int32_t heads, int64_t n_tokens,
+                           int32_t head_dim, int64_t chunk, float scale, int32_t causal,
+                           void *q_dev, float *k_dev, float *v_dev, void *k8, void *v8,
+                           int64_t plane_stride_bytes, float *m, float *l, float *o,
+                           void *out_dev, void *compute_stream, void *copy_stream);
 
 /*
  * q8a_device_status -- read (and optionally clear) the status word of the

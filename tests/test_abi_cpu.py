@@ -132,6 +132,22 @@ def test_split_step_validation(lib):
     assert call(kv_len=0, ws=P(0), ws_n=0) == Q.Q8A_OK
 
 
+def test_pipelined_prefill_validation(lib):
+    """attn_prefill_pipelined checks sizes and pointers before any CUDA call."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+
+    def call(chunk=256, hd=64, q=A16, B=1, M=512):
+        return lib.attn_prefill_pipelined(q, A16, A16, A16, B, 2, M, hd, chunk, 0.125, 1, A16, A16, A16,
+                                          A16, A16, 34816, A16, A16, A16, A16, P(0), P(0))
+
+    assert call(chunk=0) == Q.Q8A_ERR_INVALID_ARG
+    assert call(chunk=6) == Q.Q8A_ERR_INVALID_ARG
+    assert call(hd=128) == Q.Q8A_ERR_INVALID_ARG
+    assert call(q=P(0)) == Q.Q8A_ERR_INVALID_ARG
+    assert call(B=0) == Q.Q8A_OK
+    assert call(M=0) == Q.Q8A_OK
+
+
 def test_runtime_knobs_validation(lib):
     from chunked_prefill_attention_gb300 import q8attn as Q
     assert lib.q8a_set_wait_timeout_ns(10) == Q.Q8A_ERR_INVALID_ARG
