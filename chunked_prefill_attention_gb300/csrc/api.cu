@@ -192,6 +192,7 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
   a->scale = scale;
   a->scale_log2 = scale * 1.4426950408889634f;
   a->causal = causal ? 1 : 0;
+  a->pair = (!causal && n_qtiles == 1) ? 1 : 0;
   a->timeout_ns = g_timeout_ns.load();
   return Q8A_OK;
 }

@@ -83,19 +83,28 @@ constexpr int OFF_BAR = OFF_RAW + NR * 2 * RAWB;
 constexpr int B_QFULL = 0;
 constexpr int B_RAWFULL = 1;                 // NR
 constexpr int B_RAWEMPTY = B_RAWFULL + NR;   // NR
-constexpr int B_DEQFULL = B_RAWEMPTY + NR;   // ND
-constexpr int B_DEQEMPTY = B_DEQFULL + ND;   // ND
-constexpr int B_SFULL = B_DEQEMPTY + ND;     // NQT
+// K and V of a dequantised stage are filled and released separately: the K
+// half is free once the QKs reading it have completed (which is early: the
+// softmax of that key tile has not started yet), the V half once its PVs have.
+constexpr int B_KFULL = B_RAWEMPTY + NR;     // ND
+constexpr int B_KEMPTY = B_KFULL + ND;       // ND
+constexpr int B_VFULL = B_KEMPTY + ND;       // ND
+constexpr int B_VEMPTY = B_VFULL + ND;       // ND
+constexpr int B_SFULL = B_VEMPTY + ND;       // NQT
 constexpr int B_PFULL = B_SFULL + NQT;       // 2 x NQT: P_x keys 0-63, then keys 64-127
 constexpr int B_ODONE = B_PFULL + 2 * NQT;   // NQT
-constexpr int B_DRAIN = B_ODONE + NQT;
+constexpr int B_MERGE = B_ODONE + NQT;       // paired mode: tile B's final (m, l) published
+constexpr int B_DRAIN = B_MERGE + 1;
 constexpr int NBAR = B_DRAIN + 1;
-constexpr int OFF_CTL = OFF_BAR + NBAR * 8;
-constexpr int SMEM_USED = OFF_CTL + 16;
+constexpr int OFF_CTL = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
+constexpr int CTL_BYTES = 32;                // struct Ctl, padded
+constexpr int OFF_XCH = OFF_CTL + CTL_BYTES;  // paired mode: 128 x float4 {m, l, ok, -} of tile B
+constexpr int SMEM_USED = OFF_XCH + BM * 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;           // alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_RAW % 16 == 0 && RAWB % 16 == 0, "bulk copy alignment");
 static_assert(OFF_DEQ % 1024 == 0 && DEQ_BYTES % 1024 == 0, "swizzle atom alignment");
+static_assert(OFF_BAR % 8 == 0 && OFF_XCH % 16 == 0, "mbarrier and 16-byte exchange-slot alignment");
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_S = 0;      // + 128 * tile
@@ -110,6 +119,7 @@ struct Ctl {
   uint32_t tmem_base;
   uint32_t abort;
 };
+static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
 
 __device__ __forceinline__ bool budget_ran_out(Ctl* ctl, long long t0, uint64_t budget_cycles,
                                                uint32_t role) {
@@ -245,11 +255,26 @@ __device__ __forceinline__ Range make_range(const ChunkArgs& a) {
 }
 
 // Per-CTA work description.
+//
+// Paired mode (a.pair: one 128-row query tile per (b, h), no causal mask, as in
+// burst verification): both softmax pipelines work on the same query rows, tile
+// A on the even key tiles of the range and tile B on the odd ones, each with its
+// own running state; tile A merges B's state into its own at the end.  The two
+// pipelines then overlap exactly as two query tiles do in prefill, instead of
+// one pipeline waiting out its own softmax -> PV -> QK chain.
 struct Unit {
   int64_t bh, b, h, r0;   // (batch*heads index), first row of tile A
-  int T[NQT];             // key tiles each query tile needs (0 = inactive)
-  int T_all;              // max over tiles
+  int T[NQT];             // key tiles each query tile processes (0 = inactive)
+  int T_all;              // key tiles streamed through the CTA
 };
+
+// Query row offset of tile x from u.r0, and the key tile of tile x's j-th step.
+__device__ __forceinline__ int64_t tile_row0(const ChunkArgs& a, int x) {
+  return a.pair ? 0 : static_cast<int64_t>(x) * BM;
+}
+__device__ __forceinline__ int key_tile(const ChunkArgs& a, int x, int j) {
+  return a.pair ? 2 * j + x : j;
+}
 
 __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
@@ -260,6 +285,13 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   u.h = u.bh % a.heads;
   u.r0 = static_cast<int64_t>(a.tile0) * BM + qu * (NQT * BM);
   u.T_all = 0;
+  if (a.pair) {
+    const int tiles = kr.kv_len > 0 ? static_cast<int>((kr.kv_len + BN - 1) / BN) : 0;
+    u.T[0] = (tiles + 1) / 2;
+    u.T[1] = tiles / 2;
+    u.T_all = tiles;
+    return u;
+  }
 #pragma unroll
   for (int x = 0; x < NQT; ++x) {
     const int64_t rx = u.r0 + x * BM;
@@ -295,7 +327,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
       for (int x = 0; x < NQT; ++x)
         if (u.T[x] > 0)
           tma_load_3d(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL),
-                      static_cast<int32_t>(u.h * kHeadDim), static_cast<int32_t>(u.r0 + x * BM),
+                      static_cast<int32_t>(u.h * kHeadDim), static_cast<int32_t>(u.r0 + tile_row0(a, x)),
                       static_cast<int32_t>(u.b));
     }
   }
@@ -392,18 +424,23 @@ __device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Range& kr
   const int row_off = (k >> 3) * 1024 + (k & 7) * 128;
   for (int t = 0; t < u.T_all; ++t) {
     const int sr = t % NR, sd = t % ND;
+    const uint32_t fill = (t / ND) & 1;
     if (!wait_bar(bar(B_RAWFULL + sr), (t / NR) & 1, ctl, budget, R_DEQUANT, true)) break;
-    if (!wait_bar(bar(B_DEQEMPTY + sd), ((t / ND) & 1) ^ 1, ctl, budget, R_DEQUANT, true))
-      break;
     const int n_valid = static_cast<int>(i64min(BN, kr.kv_len - static_cast<int64_t>(t) * BN));
     uint8_t* dq = smem + OFF_DEQ + sd * DEQ_BYTES + row_off;
-    if (k < n_valid) {
+    bool stop = false;
 #pragma unroll 1
-      for (int tensor = 0; tensor < 2; ++tensor) {   // K, then V
+    for (int tensor = 0; tensor < 2; ++tensor) {   // K, then V
+      if (!wait_bar(bar((tensor ? B_VEMPTY : B_KEMPTY) + sd), fill ^ 1, ctl, budget, R_DEQUANT,
+                    true)) {
+        stop = true;
+        break;
+      }
+      uint8_t* hi_row = dq + (tensor ? DQ_VHI : DQ_KHI);
+      uint8_t* lo_row = dq + (tensor ? DQ_VLO : DQ_KLO);
+      if (k < n_valid) {
         const uint32_t* raw = reinterpret_cast<const uint32_t*>(
             smem + OFF_RAW + sr * 2 * RAWB + tensor * RAWB + k * kRowBytes);
-        uint8_t* hi_row = dq + (tensor ? DQ_VHI : DQ_KHI);
-        uint8_t* lo_row = dq + (tensor ? DQ_VLO : DQ_KLO);
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
           uint32_t w[9];
@@ -411,19 +448,18 @@ __device__ __forceinline__ void dequant_role(const ChunkArgs& a, const Range& kr
           for (int i = 0; i < 9; ++i) w[i] = raw[8 * blk + i];
           dequant_block(w, blk, hi_row, lo_row, sw);
         }
-      }
-    } else {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4*>(dq + DQ_KHI + 16 * c) = z;
-        *reinterpret_cast<uint4*>(dq + DQ_KLO + 16 * c) = z;
-        *reinterpret_cast<uint4*>(dq + DQ_VHI + 16 * c) = z;
-        *reinterpret_cast<uint4*>(dq + DQ_VLO + 16 * c) = z;
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(hi_row + 16 * c) = z;
+          *reinterpret_cast<uint4*>(lo_row + 16 * c) = z;
+        }
       }
+      fence_proxy_async_smem();
+      mbar_arrive(bar((tensor ? B_VFULL : B_KFULL) + sd));
     }
-    fence_proxy_async_smem();
-    mbar_arrive(bar(B_DEQFULL + sd));
+    if (stop) break;
     mbar_arrive(bar(B_RAWEMPTY + sr));
   }
 }
@@ -461,9 +497,10 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
   const uint64_t qdesc0 = smem_desc(sbase + OFF_Q, 1024, 1024, kSwizzle128);
   const uint64_t kdesc0 = smem_desc(sbase + OFF_DEQ + DQ_KHI, 1024, 1024, kSwizzle128);
   const uint64_t vdesc0 = smem_desc(sbase + OFF_DEQ + DQ_VHI, DQ_VLO - DQ_VHI, 1024, kSwizzle128);
-  auto issue_qk = [&](int x, int t) {
+  // stage sd of the dequantised ring
+  auto issue_qk = [&](int x, int sd) {
     const uint64_t qd = qdesc0 + static_cast<uint64_t>(x * (16384 >> 4));
-    const uint64_t kd = kdesc0 + static_cast<uint64_t>((t % ND) * (DEQ_BYTES >> 4));
+    const uint64_t kd = kdesc0 + static_cast<uint64_t>(sd * (DEQ_BYTES >> 4));
     const uint32_t d = tmem + T_S + 128u * x;
     if (leader) {
 #pragma unroll
@@ -474,8 +511,8 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
     }
   };
   // half h covers keys 64h .. 64h+63 (k-steps 4h .. 4h+3)
-  auto issue_pv = [&](int x, int t, int h) {
-    const uint64_t vd = vdesc0 + static_cast<uint64_t>((t % ND) * (DEQ_BYTES >> 4));
+  auto issue_pv = [&](int x, int sd, int h) {
+    const uint64_t vd = vdesc0 + static_cast<uint64_t>(sd * (DEQ_BYTES >> 4));
     const uint32_t o = tmem + T_O + 128u * x;
     const uint32_t p = tmem + T_S + 128u * x;
     if (leader) {
@@ -487,50 +524,63 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
     if (leader) mma_commit(bar(b));
   };
 
-  bool ok = wait_bar(bar(B_QFULL), 0, ctl, budget, R_MMA, true) &&
-            wait_bar(bar(B_DEQFULL + 0), 0, ctl, budget, R_MMA, true);
+  // Tile x's j-th key tile sits in stage kt % ND of the ring, filled for the
+  // (kt / ND)-th time.  In prefill both tiles read every key tile, so a
+  // stage half is released after tile B's MMA on it; in paired mode each key
+  // tile has one reader.
+  const bool pair = a.pair != 0;
+  auto stage = [&](int x, int j) { return key_tile(a, x, j) % ND; };
+  auto fill = [&](int x, int j) { return static_cast<uint32_t>((key_tile(a, x, j) / ND) & 1); };
+
+  bool ok = wait_bar(bar(B_QFULL), 0, ctl, budget, R_MMA, true);
   if (ok) {
-    tc_fence_after();
 #pragma unroll
     for (int x = 0; x < NQT; ++x)
-      if (u.T[x] > 0) {
-        issue_qk(x, 0);
+      if (ok && u.T[x] > 0) {
+        ok = wait_bar(bar(B_KFULL + stage(x, 0)), fill(x, 0), ctl, budget, R_MMA, true);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(x, stage(x, 0));
         commit(B_SFULL + x);
+        if (pair) commit(B_KEMPTY + stage(x, 0));
       }
+    if (ok && !pair) commit(B_KEMPTY + 0);   // every reader of K(0) issued
   }
-  int deq_ready = 0;   // highest key tile whose dequantised stage is known full
-  for (int t = 0; ok && t < u.T_all; ++t) {
+  const int steps = pair ? u.T[0] : u.T_all;
+  for (int j = 0; ok && j < steps; ++j) {
 #pragma unroll
     for (int x = 0; x < NQT; ++x) {
-      if (t < u.T[x]) {
-        if (!wait_bar(bar(B_PFULL + 2 * x), t & 1, ctl, budget, R_MMA, true)) {
+      if (j < u.T[x]) {
+        const int sd = stage(x, j);
+        if (!wait_bar(bar(B_VFULL + sd), fill(x, j), ctl, budget, R_MMA, true) ||
+            !wait_bar(bar(B_PFULL + 2 * x), j & 1, ctl, budget, R_MMA, true)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_pv(x, t, 0);
-        if (!wait_bar(bar(B_PFULL + 2 * x + 1), t & 1, ctl, budget, R_MMA, true)) {
+        issue_pv(x, sd, 0);
+        if (!wait_bar(bar(B_PFULL + 2 * x + 1), j & 1, ctl, budget, R_MMA, true)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_pv(x, t, 1);
-        if (t == u.T[x] - 1) commit(B_ODONE + x);
+        issue_pv(x, sd, 1);
+        if (j == u.T[x] - 1) commit(B_ODONE + x);
+        if (pair) commit(B_VEMPTY + sd);
       }
-      if (x == NQT - 1) commit(B_DEQEMPTY + t % ND);   // every reader of tile t issued
-      if (t + 1 < u.T[x]) {
-        if (deq_ready < t + 1) {
-          if (!wait_bar(bar(B_DEQFULL + (t + 1) % ND), ((t + 1) / ND) & 1, ctl, budget, R_MMA,
-                        true)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          deq_ready = t + 1;
+      if (!pair && x == NQT - 1) commit(B_VEMPTY + j % ND);   // every reader of V(j) issued
+      if (j + 1 < u.T[x]) {
+        const int sd = stage(x, j + 1);
+        if (!wait_bar(bar(B_KFULL + sd), fill(x, j + 1), ctl, budget, R_MMA, true)) {
+          ok = false;
+          break;
         }
-        issue_qk(x, t + 1);
+        tc_fence_after();
+        issue_qk(x, sd);
         commit(B_SFULL + x);
+        if (pair) commit(B_KEMPTY + sd);
       }
+      if (!pair && x == NQT - 1 && j + 1 < u.T_all) commit(B_KEMPTY + (j + 1) % ND);
     }
   }
   // Never leave with an MMA in flight.
@@ -539,8 +589,52 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
   wait_bar(bar(B_DRAIN), 0, ctl, budget, R_DRAIN, false);
 }
 
+// Paired mode: fold tile B's final state (m_b, l_b; O at TMEM address t_ob)
+// into tile A's (m_a, l_a; O at t_oa) and write the result -- the chunk
+// recurrence applied to two partial states over disjoint keys.  The weight of
+// the state holding the larger max is exactly 1.  O is the sum of each tile's
+// high and residual halves.
+__device__ __forceinline__ void merge_pair_out(const Range& kr, int64_t sidx, bool active,
+                                               float m_a, float l_a, float m_b, float l_b,
+                                               uint32_t t_oa, uint32_t t_ob) {
+  const float m = fmaxf(m_a, m_b);
+  const float wa = (m_a == m) ? 1.0f : (m_a == -INFINITY ? 0.0f : ex2_approx((m_a - m) * kLog2e));
+  const float wb = (m_b == m) ? 1.0f : (m_b == -INFINITY ? 0.0f : ex2_approx((m_b - m) * kLog2e));
+  if (active) {
+    kr.m[sidx] = m;
+    kr.l[sidx] = fmaf(wa, l_a, wb * l_b);
+  }
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ah[32], al[32], bh[32], bl[32];
+    tmem_ld32(t_oa + 32 * half, ah);
+    tmem_ld32(t_oa + 64 + 32 * half, al);
+    tmem_ld32(t_ob + 32 * half, bh);
+    tmem_ld32(t_ob + 64 + 32 * half, bl);
+    tmem_wait_ld(ah);
+    tmem_wait_ld(al);
+    tmem_wait_ld(bh);
+    tmem_wait_ld(bl);
+    if (active) {
+      float4* dst = reinterpret_cast<float4*>(kr.o + sidx * kHeadDim) + 8 * half;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * i + e;
+          const float oa = __uint_as_float(ah[c]) + __uint_as_float(al[c]);
+          const float ob = __uint_as_float(bh[c]) + __uint_as_float(bl[c]);
+          v[e] = fmaf(wa, oa, wb * ob);
+        }
+        dst[i] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr, const Unit& u, int x,
-                                             uint32_t sbase, uint32_t tmem, Ctl* ctl) {
+                                             uint8_t* smem, uint32_t sbase, uint32_t tmem, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;   // cycles
   const int row = threadIdx.x & 127;       // TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;   // warp's lane quarter
@@ -549,22 +643,25 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
   const int T = u.T[x];
   if (T == 0) return;
 
-  const int64_t rg = u.r0 + x * BM + row;
+  const int64_t rg = u.r0 + tile_row0(a, x) + row;
   const int64_t pos = a.q_pos0 + rg;
   const bool active = rg < a.n_q && (!a.causal || pos >= kr.kv_start);
   const int64_t sidx = u.bh * a.n_q + rg;
   const uint32_t t_s = tmem + lane_off + T_S + 128u * x;
   const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
 
+  // in paired mode tile B starts from the empty state and tile A merges it in
+  const bool fresh = kr.fresh || (a.pair && x == 1);
+  const bool pair_merge = a.pair && u.T[1] > 0;
   float m_run = -INFINITY, l_run = 0.0f;
-  if (active && !kr.fresh) {
+  if (active && !fresh) {
     m_run = kr.m[sidx];
     l_run = kr.l[sidx];
   }
   {
     // the O row enters TMEM as the high half; the residual half starts at 0
     uint32_t oh[64];
-    if (active && !kr.fresh) {
+    if (active && !fresh) {
       const float4* src = reinterpret_cast<const float4*>(kr.o + sidx * kHeadDim);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -588,7 +685,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
   }
 
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
-  const int64_t q_first = a.q_pos0 + u.r0 + x * BM;   // position of the tile's first row
+  const int64_t q_first = a.q_pos0 + u.r0 + tile_row0(a, x);   // position of the tile's first row
   bool ok = true;
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {
@@ -607,7 +704,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
     tmem_wait_ld_at<64>(s);
     tmem_wait_ld_at<96>(s);
 
-    const int64_t k0 = static_cast<int64_t>(t) * BN;
+    const int64_t k0 = static_cast<int64_t>(key_tile(a, x, t)) * BN;
     const bool need_mask = (k0 + BN > kr.kv_len) || (a.causal && kr.kv_start + k0 + BN - 1 > q_first);
     if (__builtin_expect(need_mask, 0)) {
       int64_t lim = kr.kv_len - 1 - k0;
@@ -689,9 +786,26 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
     const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
     l_run = fmaf(l_run, alpha, r.x + r.y);   // same ops per tile with or without chunking
   }
+  float4* xch = reinterpret_cast<float4*>(smem + OFF_XCH) + row;
+  if (pair_merge && x == 1) {
+    // publish (m, l) for tile A, which reads this tile's O from TMEM itself
+    *xch = make_float4(m_run, l_run, ok ? 1.0f : 0.0f, 0.0f);
+    mbar_arrive(bar(B_MERGE));
+    return;
+  }
   if (ok) {
     if (wait_bar(bar(B_ODONE + x), 0, ctl, budget, R_SOFTMAX, true)) {
       tc_fence_after();
+      if (pair_merge) {
+        if (!wait_bar(bar(B_MERGE), 0, ctl, budget, R_SOFTMAX, true) ||
+            !wait_bar(bar(B_ODONE + 1), 0, ctl, budget, R_SOFTMAX, true))
+          return;
+        tc_fence_after();
+        const float4 pb = *xch;
+        if (pb.z == 0.0f) return;   // tile B gave up; the failure is already recorded
+        merge_pair_out(kr, sidx, active, m_run, l_run, pb.x, pb.y, t_o, t_o + 128u);
+        return;
+      }
       if (active) {
         kr.m[sidx] = m_run;
         kr.l[sidx] = l_run;
@@ -737,7 +851,9 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t count = 1;
       if (i >= B_RAWEMPTY && i < B_RAWEMPTY + NR) count = 128;   // dequant threads
-      if (i >= B_DEQFULL && i < B_DEQFULL + ND) count = 128;     // dequant threads
+      if (i >= B_KFULL && i < B_KFULL + ND) count = 128;         // dequant threads
+      if (i >= B_VFULL && i < B_VFULL + ND) count = 128;         // dequant threads
+      if (i == B_MERGE) count = 128;                             // softmax threads of tile B
       if (i >= B_PFULL && i < B_PFULL + 2 * NQT) count = 128;    // softmax threads of a tile
       mbar_init(sbase + OFF_BAR + 8u * i, count);
     }
@@ -757,7 +873,7 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   // fragments; the other warpgroups need far fewer registers.
   if (wg < 2) {
     reg_alloc<kRegSoftmax>();
-    softmax_role(a, kr, u, wg, sbase, tmem, ctl);
+    softmax_role(a, kr, u, wg, smem, sbase, tmem, ctl);
   } else {
     reg_dealloc<kRegOther>();
     if (wg == 2) {

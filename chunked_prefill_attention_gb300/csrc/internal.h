@@ -42,6 +42,8 @@ struct ChunkArgs {
   float scale_log2;       // scale * log2(e)
   int32_t causal;
   int32_t inject;         // test hook: 1 = first block skips its query-tile load
+  int32_t pair;           // 1: one query tile, no causal mask -- the CTA's two softmax
+                          // pipelines share the rows and split the key tiles (even / odd)
   uint64_t timeout_ns;    // budget of every device-side wait
   // Split form (split_keys > 0): block row y of the grid folds keys
   // [y*split_keys, min((y+1)*split_keys, kv_len)) of the chunk into an empty
