@@ -186,6 +186,7 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
   a->kv_len = kv_len;
   a->n_q = n_q;
   a->heads = heads;
+  a->kv_heads = heads;
   a->bh = static_cast<int32_t>(batch * heads);
   a->tile0 = static_cast<int32_t>(tile0);
   a->n_qtiles = static_cast<int32_t>(n_qtiles);
@@ -223,6 +224,29 @@ int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, in
   if (batch < 0 || heads <= 0 || n_q < 0 || kv_len < 0 || split_keys <= 0) return -1;
   const int64_t n_splits = (kv_len + split_keys - 1) / split_keys;
   return n_splits * batch * heads * n_q * (Q8A_HEAD_DIM + 2);
+}
+
+int attn_chunk_step_gqa(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                        int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
+                        float* l, float* o, int64_t batch, int32_t heads, int32_t kv_heads,
+                        int64_t n_q, int32_t head_dim, float scale, int32_t causal, void* stream) {
+  const char* fn = "attn_chunk_step_gqa";
+  if (kv_heads <= 0 || heads <= 0 || heads % kv_heads != 0)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: heads (%d) must be a positive multiple of kv_heads (%d)",
+                fn, (int)heads, (int)kv_heads);
+  CUtensorMap qmap;
+  q8a::ChunkArgs a;
+  bool empty = false;
+  if (int rc = prepare_chunk_step(fn, q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start,
+                                  kv_len, m, l, o, batch, heads, n_q, head_dim, scale, causal,
+                                  &qmap, &a, &empty))
+    return rc;
+  if (empty) return ok();
+  a.kv_heads = kv_heads;
+  a.inject = g_inject.exchange(0);
+  cudaError_t e = q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
 }
 
 int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,

@@ -335,8 +335,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
 #pragma unroll
   for (int s = 0; s < NR; ++s) last_bulk[s] = -1;
 
-  const uint8_t* kp = kr.k8 + u.bh * a.plane_stride;
-  const uint8_t* vp = kr.v8 + u.bh * a.plane_stride;
+  // K/V plane of this query head (grouped-query attention: heads / kv_heads
+  // query heads share one plane)
+  const int64_t kv_plane = u.b * a.kv_heads + u.h / (a.heads / a.kv_heads);
+  const uint8_t* kp = kr.k8 + kv_plane * a.plane_stride;
+  const uint8_t* vp = kr.v8 + kv_plane * a.plane_stride;
   for (int t = 0; t < u.T_all; ++t) {
     const int sr = t % NR;
     if (!wait_bar(bar(B_RAWEMPTY + sr), ((t / NR) & 1) ^ 1, ctl, budget, R_PRODUCER, true))

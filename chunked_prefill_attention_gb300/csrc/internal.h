@@ -35,6 +35,7 @@ struct ChunkArgs {
   int64_t kv_len;         // keys in the chunk (> 0)
   int64_t n_q;            // query rows per (b,h)
   int32_t heads;
+  int32_t kv_heads;       // K/V heads (planes per batch entry); heads is a multiple of it
   int32_t bh;             // batch * heads
   int32_t tile0;          // first 128-row query tile launched
   int32_t n_qtiles;       // 128-row query tiles launched per (b,h), from tile0 on

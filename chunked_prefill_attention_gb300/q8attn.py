@@ -36,6 +36,8 @@ SIGNATURES = {
     "attn_state_init": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
     "attn_chunk_step": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32,
                                        _I64, _I32, _F, _I32, _P]),
+    "attn_chunk_step_gqa": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
+                                           _I32, _I32, _I64, _I32, _F, _I32, _P]),
     "attn_chunk_step_split": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
                                              _I32, _I64, _I32, _F, _I32, _I64, _P, _I64, _P]),
     "q8a_split_workspace_floats": (_I64, [_I64, _I32, _I64, _I64, _I64]),
@@ -143,6 +145,26 @@ def attn_chunk_step(q, k8, v8, kv_start, kv_len, state, q_pos0=0, scale=None, ca
     _check(lib.attn_chunk_step(_ptr(q), q_pos0, kp, vp, stride, kv_start, kv_len, _ptr(state.m),
                                _ptr(state.l), _ptr(state.o), B, H, n_q, D, scale, int(bool(causal)),
                                _stream(q)))
+    return state
+
+
+def attn_chunk_step_gqa(q, k8, v8, kv_start, kv_len, state, q_pos0=0, scale=None, causal=True,
+                        stride=None, k_offset_bytes=0):
+    """attn_chunk_step for grouped-query attention: k8, v8 hold kv_heads =
+    k8.shape[1] planes per batch entry and query head h reads plane
+    h // (H // kv_heads)."""
+    B, n_q, H, D = q.shape
+    kv_heads = k8.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stride is None:
+        stride = k8.shape[-1]
+    lib = load()
+    kp = ctypes.c_void_p(k8.data_ptr() + k_offset_bytes)
+    vp = ctypes.c_void_p(v8.data_ptr() + k_offset_bytes)
+    _check(lib.attn_chunk_step_gqa(_ptr(q), q_pos0, kp, vp, stride, kv_start, kv_len, _ptr(state.m),
+                                   _ptr(state.l), _ptr(state.o), B, H, kv_heads, n_q, D, scale,
+                                   int(bool(causal)), _stream(q)))
     return state
 
 

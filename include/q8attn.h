@@ -139,6 +139,25 @@ int attn_chunk_step(const void *q, int64_t q_pos0, const void *k_q8, const void 
                     void *stream);
 
 /*
+ * attn_chunk_step_gqa -- attn_chunk_step for grouped-query attention: `heads`
+ * query heads share `kv_heads` K/V heads, query head h reading K/V head
+ * h / (heads / kv_heads) (so kv_heads = heads is attn_chunk_step and
+ * kv_heads = 1 is multi-query attention).  Grouping is not on the source pages;
+ * it is the standard layout of models whose KV cache has fewer heads than the
+ * queries, and it shrinks the Q8_0 cache by heads / kv_heads.  Arguments as for
+ * attn_chunk_step, except that k_q8 and v_q8 hold batch * kv_heads planes
+ * (plane (b, g) starts kv_plane_stride_bytes*(b*kv_heads+g) later) while q and
+ * the state keep `heads` heads.
+ * Errors: as attn_chunk_step; Q8A_ERR_INVALID_ARG also when kv_heads <= 0 or
+ * heads is not a multiple of kv_heads.
+ */
+int attn_chunk_step_gqa(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,
+                        int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                        float *m, float *l, float *o, int64_t batch, int32_t heads,
+                        int32_t kv_heads, int64_t n_q, int32_t head_dim, float scale,
+                        int32_t causal, void *stream);
+
+/*
  * attn_chunk_step_split -- the same update as attn_chunk_step for query rows
  * that are few against a long chunk, such as Mode B speculative burst
  * verification ([STREAM §4]: K = 64 candidate queries against the whole

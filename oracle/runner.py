@@ -7,6 +7,7 @@ holds a CUDA context.  Each task is one (batch, head) plane or one slice of a
 tensor, so the per-task memory stays bounded.
 """
 
+import atexit
 import multiprocessing as mp
 import os
 
@@ -33,6 +34,7 @@ def pool():
         os.environ.update({v: "1" for v in _BLAS_VARS})
         try:
             _POOL = mp.get_context("spawn").Pool(workers())
+            atexit.register(_close_pool)
         finally:
             for v, old in saved.items():
                 if old is None:
@@ -40,6 +42,15 @@ def pool():
                 else:
                     os.environ[v] = old
     return _POOL
+
+
+def _close_pool():
+    """Stop the workers before the interpreter tears down the pool's queues."""
+    global _POOL
+    if _POOL is not None:
+        _POOL.terminate()
+        _POOL.join()
+        _POOL = None
 
 
 def _quant_task(x):
@@ -72,16 +83,25 @@ def _attn_task(args):
 def attention(q, k8, v8, scale, causal=True, rows=None, q_pos0=0):
     """Plain-definition attention on oracle-quantised KV, per (b, h) plane.
 
-    q: fp16 numpy [B, n_q, H, 64]; k8, v8: uint8 [B, H, M, 68] (oracle bytes).
+    q: fp16 numpy [B, n_q, H, 64]; k8, v8: uint8 [B, H_kv, M, 68] (oracle
+    bytes) with H a multiple of H_kv.  Query head h attends over K/V head
+    h // (H // H_kv): grouped-query attention, which the source pages do not
+    describe; it is the standard definition (H_kv = H is ordinary multi-head
+    attention, H_kv = 1 multi-query attention).
     rows: optional query-row indices (same for every plane).
     Returns fp64 [B, len(rows) or n_q, H, 64]."""
     B, n_q, H, D = q.shape
+    H_kv = k8.shape[1]
+    if H_kv <= 0 or H % H_kv != 0:
+        raise ValueError(f"query heads {H} are not a multiple of K/V heads {H_kv}")
+    group = H // H_kv
     rows = np.arange(n_q) if rows is None else np.asarray(rows, dtype=np.int64)
     tasks = []
     for b in range(B):
         for h in range(H):
+            g = h // group
             kv_need = k8.shape[2] if not causal else min(k8.shape[2], q_pos0 + int(rows.max()) + 1)
-            tasks.append((q[b, rows, h].astype(np.float64), rows, k8[b, h, :kv_need], v8[b, h, :kv_need],
+            tasks.append((q[b, rows, h].astype(np.float64), rows, k8[b, g, :kv_need], v8[b, g, :kv_need],
                           scale, causal, q_pos0))
     res = pool().map(_attn_task, tasks, chunksize=1)
     out = np.zeros((B, rows.size, H, D), dtype=np.float64)

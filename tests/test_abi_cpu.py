@@ -108,6 +108,27 @@ def test_chunk_step_validation(lib):
     assert call(kv_start=128, n_q=128) == Q.Q8A_OK
 
 
+def test_gqa_step_validation(lib):
+    """attn_chunk_step_gqa rejects a head count that is not a multiple of the
+    K/V head count before any CUDA call; otherwise it validates like
+    attn_chunk_step."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    s = P(0)
+
+    def call(heads=4, kv_heads=2, k=A16, kv_len=128, hd=64, n_q=128):
+        return lib.attn_chunk_step_gqa(A16, 0, k, A16, 8704, 0, kv_len, A16, A16, A16, 1, heads,
+                                       kv_heads, n_q, hd, 0.125, 1, s)
+
+    assert call(kv_heads=0) == Q.Q8A_ERR_INVALID_ARG
+    assert call(kv_heads=-2) == Q.Q8A_ERR_INVALID_ARG
+    assert call(heads=6, kv_heads=4) == Q.Q8A_ERR_INVALID_ARG
+    assert call(heads=2, kv_heads=4) == Q.Q8A_ERR_INVALID_ARG
+    assert call(hd=32) == Q.Q8A_ERR_UNSUPPORTED
+    assert call(k=P(0)) == Q.Q8A_ERR_INVALID_ARG
+    assert call(kv_len=0, k=P(0)) == Q.Q8A_OK
+    assert call(n_q=0) == Q.Q8A_OK
+
+
 def test_split_step_validation(lib):
     """attn_chunk_step_split rejects bad range sizes and workspaces before it
     touches the device."""

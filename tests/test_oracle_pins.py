@@ -340,3 +340,50 @@ def test_row_without_visible_key_finalises_to_zero():
     att.chunk_step(st, q, k, v, 5, 0.5)
     assert np.all(np.isneginf(st["m"])) and np.all(st["l"] == 0)
     assert np.array_equal(att.finalize(st), np.zeros((3, 4)))
+
+
+# ---- grouped-query attention (an extension: the pages describe one K/V head
+# per query head; query head h of H reads K/V head h // (H / H_kv)) ----------
+
+def _gqa_case(H, H_kv, M=48, seed=7):
+    from oracle import runner
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((1, M, H, 64)).astype(np.float16)
+    k = rng.standard_normal((1, M, H_kv, 64)).astype(np.float32)
+    v = rng.standard_normal((1, M, H_kv, 64)).astype(np.float32)
+    return q, runner.quantize_kv(k, parallel=False), runner.quantize_kv(v, parallel=False)
+
+
+@pytest.mark.parametrize("H,H_kv", [(4, 2), (6, 3), (4, 1)])
+def test_gqa_equals_multi_head_on_repeated_kv(H, H_kv):
+    """Grouped heads give exactly what multi-head attention gives when every
+    K/V plane is repeated for the H / H_kv query heads of its group."""
+    from oracle import runner
+    q, k8, v8 = _gqa_case(H, H_kv)
+    got = runner.attention(q, k8, v8, 0.125)
+    rep = H // H_kv
+    want = runner.attention(q, np.repeat(k8, rep, axis=1), np.repeat(v8, rep, axis=1), 0.125)
+    assert np.array_equal(got, want)
+    # and not what an interleaved (h % H_kv) assignment would give
+    if H_kv > 1 and rep > 1:
+        inter = runner.attention(q, np.tile(k8, (1, rep, 1, 1)), np.tile(v8, (1, rep, 1, 1)), 0.125)
+        assert not np.allclose(got, inter)
+
+
+def test_mqa_identical_queries_give_identical_heads():
+    """One K/V head shared by all query heads: heads with the same queries
+    produce the same output."""
+    from oracle import runner
+    q, k8, v8 = _gqa_case(4, 1)
+    q[:, :, 1] = q[:, :, 0]
+    q[:, :, 3] = q[:, :, 0]
+    out = runner.attention(q, k8, v8, 0.125)
+    assert np.array_equal(out[:, :, 1], out[:, :, 0]) and np.array_equal(out[:, :, 3], out[:, :, 0])
+    assert not np.allclose(out[:, :, 2], out[:, :, 0])
+
+
+def test_gqa_rejects_ungrouped_heads():
+    from oracle import runner
+    q, k8, v8 = _gqa_case(4, 2)
+    with pytest.raises(ValueError):
+        runner.attention(q[:, :, :3], k8, v8, 0.125)
