@@ -30,7 +30,9 @@
 //              converted by the exponent-bias trick), so every tensor-core
 //              operand is exact.  The four 128 x 64 fp16 tiles (K_hi, K_lo,
 //              V_hi, V_lo) are written with the 128-byte swizzle, one key per
-//              128-byte row.
+//              128-byte row.  The K and V halves of a stage are filled and
+//              released on separate barriers: K is free once its QKs are done,
+//              before the softmax of that key tile starts.
 //   WG3        warp 12: producer -- TMA tensor loads of the two fp16 Q tiles and
 //              cp.async.bulk of the raw 68-byte-row K/V tiles (8704 B each,
 //              contiguous in the head-major planes) into a 2-stage ring;
@@ -44,6 +46,11 @@
 //          are added when the state is written back.
 // Issue order (ping-pong): PV_A(t), QK_A(t+1), PV_B(t), QK_B(t+1), ... so the
 // tensor pipe works on one tile while the other tile's softmax runs.
+// Paired mode (one 128-row query tile, no causal mask, e.g. burst
+// verification): both pipelines take the same rows, A the even and B the odd
+// key tiles, and A merges B's state at the end, so the ping-pong still has two
+// chains to interleave.  Grouped-query attention only changes the K/V plane a
+// CTA streams: query head h reads plane h / (heads / kv_heads).
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Every mbarrier wait is bounded by a budget; a wait that runs out records the
 // failing role in a per-device status word, every role then leaves its loop,

@@ -21,6 +21,10 @@ cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, cudaSt
 // attn_finalize: fp32 O, l -> fp16 out [B][n_q][H][64].
 cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
                             int32_t heads, int64_t n_q, cudaStream_t stream);
+// The same for query rows row0 .. row0+n_rows-1 of every (b, h) plane only.
+cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int64_t batch,
+                                 int32_t heads, int64_t n_q, int64_t row0, int64_t n_rows,
+                                 cudaStream_t stream);
 
 // Arguments of one chunk-step launch (everything but the Q tensor map).
 struct ChunkArgs {

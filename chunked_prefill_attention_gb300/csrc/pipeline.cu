@@ -48,15 +48,35 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
   cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
   const int64_t row_floats = static_cast<int64_t>(heads) * Q8A_HEAD_DIM;   // one token, all heads
   const size_t q_bytes = static_cast<size_t>(batch * n_tokens * row_floats) * 2;
-  const size_t out_bytes = q_bytes;
 
-  cudaEvent_t ev = nullptr;
+  // ev: a chunk's inputs are on the device (copy stream -> compute stream);
+  // ev_fin: a row block of the output is final (compute stream -> copy stream).
+  cudaEvent_t ev = nullptr, ev_fin = nullptr;
   cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
   if (e != cudaSuccess) return cuda_err(e, "cudaEventCreateWithFlags");
+  e = cudaEventCreateWithFlags(&ev_fin, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaEventDestroy(ev);
+    return cuda_err(e, "cudaEventCreateWithFlags");
+  }
   int rc = Q8A_OK;
   auto bail = [&](int code) {
     cudaEventDestroy(ev);   // released once the recorded work is done
+    cudaEventDestroy(ev_fin);
     return code;
+  };
+  const size_t out_row_bytes = static_cast<size_t>(row_floats) * 2;   // one token, all heads, fp16
+  // copy query rows [r0, r0 + n) of every sequence back to the host on `st`
+  auto copy_out_rows = [&](int64_t r0, int64_t n, cudaStream_t st) -> cudaError_t {
+    for (int64_t b = 0; b < batch; ++b) {
+      const size_t off = static_cast<size_t>(b * n_tokens + r0) * out_row_bytes;
+      cudaError_t ce = cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + off,
+                                       static_cast<const uint8_t*>(out_dev) + off,
+                                       static_cast<size_t>(n) * out_row_bytes,
+                                       cudaMemcpyDeviceToHost, st);
+      if (ce != cudaSuccess) return ce;
+    }
+    return cudaSuccess;
   };
   // Earlier work on the compute stream may still read the device buffers that
   // the copies below overwrite: the copy stream starts after it.
@@ -66,6 +86,11 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
     return bail(cuda_err(e, "copy of Q"));
   if ((rc = attn_state_init(m, l, o, batch, heads, n_tokens, head_dim, cs)) != Q8A_OK) return bail(rc);
 
+  // With the causal mask (q_pos0 = 0) no later chunk touches the query rows of
+  // chunk c, so they are final once its step has run: they are finalised then,
+  // and copied back on the copy stream behind the next chunk's inputs, while
+  // the device works on the chunks after it.
+  int64_t prev_r0 = -1, prev_n = 0;   // row block finalised but not yet copied back
   for (int64_t s0 = 0; s0 < n_tokens; s0 += chunk) {
     const int64_t n = (n_tokens - s0 < chunk) ? n_tokens - s0 : chunk;
     const size_t bytes = static_cast<size_t>(n * row_floats) * sizeof(float);
@@ -77,6 +102,12 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
     }
     // the chunk (and, before it on the copy stream, Q) is on the device once ev fires
     if ((e = cudaEventRecord(ev, xs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+    if (prev_r0 >= 0) {
+      if ((e = cudaStreamWaitEvent(xs, ev_fin, 0)) != cudaSuccess ||
+          (e = copy_out_rows(prev_r0, prev_n, xs)) != cudaSuccess)
+        return bail(cuda_err(e, "copy of an output row block"));
+      prev_r0 = -1;
+    }
     if ((e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
     for (int64_t b = 0; b < batch; ++b) {
       const int64_t off = (b * n_tokens + s0) * row_floats;
@@ -90,10 +121,25 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
                               static_cast<const uint8_t*>(v8) + s0 * Q8A_ROW_BYTES, plane_stride_bytes,
                               s0, n, m, l, o, batch, heads, n_tokens, head_dim, scale, causal, cs)) != Q8A_OK)
       return bail(rc);
+    if (causal) {
+      if ((e = q8a::launch_finalize_rows(l, o, out_dev, batch, heads, n_tokens, s0, n, cs)) != cudaSuccess)
+        return bail(cuda_err(e, "finalize of a row block"));
+      if ((e = cudaEventRecord(ev_fin, cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+      prev_r0 = s0;
+      prev_n = n;
+    }
+  }
+  if (causal) {
+    // the last row block, then the compute stream waits for every copy back
+    if ((e = cudaStreamWaitEvent(xs, ev_fin, 0)) != cudaSuccess ||
+        (e = copy_out_rows(prev_r0, prev_n, xs)) != cudaSuccess)
+      return bail(cuda_err(e, "copy of an output row block"));
+    if ((e = cudaEventRecord(ev, xs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+    if ((e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
+    return bail(Q8A_OK);
   }
   if ((rc = attn_finalize(l, o, out_dev, batch, heads, n_tokens, head_dim, cs)) != Q8A_OK) return bail(rc);
-  if ((e = cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
-    return bail(cuda_err(e, "copy of the output"));
+  if ((e = copy_out_rows(0, n_tokens, cs)) != cudaSuccess) return bail(cuda_err(e, "copy of the output"));
   return bail(Q8A_OK);
 }
 

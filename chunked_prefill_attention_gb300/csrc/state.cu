@@ -35,14 +35,16 @@ state_init_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restri
 
 __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4* __restrict__ out,
-                int64_t n_q, int32_t heads, int64_t rows) {
+                int64_t n_q, int32_t heads, int64_t row0, int64_t n_rows, int64_t rows) {
+  // rows = B*H*n_rows state rows: query rows row0 .. row0+n_rows-1 of every plane
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * 8;
        g += stride) {
-    const int64_t row = g >> 3;         // (b*H + h)*n_q + r
+    const int64_t k = g >> 3;           // (b*H + h)*n_rows + (r - row0)
     const int part = static_cast<int>(g & 7);
-    const int64_t r = row % n_q;
-    const int64_t bh = row / n_q;
+    const int64_t r = row0 + k % n_rows;
+    const int64_t bh = k / n_rows;
+    const int64_t row = bh * n_q + r;   // (b*H + h)*n_q + r
     const int64_t h = bh % heads;
     const int64_t b = bh / heads;
     const float lv = __ldg(l + row);
@@ -140,10 +142,17 @@ cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, cudaSt
 
 cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
                             int32_t heads, int64_t n_q, cudaStream_t stream) {
-  const int64_t rows = batch * heads * n_q;
+  return launch_finalize_rows(l, o, out, batch, heads, n_q, 0, n_q, stream);
+}
+
+cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int64_t batch,
+                                 int32_t heads, int64_t n_q, int64_t row0, int64_t n_rows,
+                                 cudaStream_t stream) {
+  const int64_t rows = batch * heads * n_rows;
   if (rows <= 0) return cudaSuccess;
   finalize_kernel<<<grid_for(rows * 8), kThreads, 0, stream>>>(
-      l, reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, rows);
+      l, reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, row0,
+      n_rows, rows);
   return cudaGetLastError();
 }
 

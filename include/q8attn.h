@@ -235,9 +235,12 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  * Q is copied to the device, then for each chunk of `chunk` tokens its K and V
  * are copied on `copy_stream` while `compute_stream` quantises and folds the
  * chunks before it (q8kv_quantize on the chunk's tokens, attn_chunk_step with
- * kv_start = the chunk's first token, q_pos0 = 0); finally attn_finalize and
- * the copy of the output back to the host.  The result is bit-identical to
- * quantising the whole K and V and folding the same chunks in order.
+ * kv_start = the chunk's first token, q_pos0 = 0).  With `causal` no later
+ * chunk touches a chunk's own query rows, so those rows are finalised right
+ * after its step and copied back to the host on copy_stream while the device
+ * works on the later chunks; without it, attn_finalize and one copy back run
+ * at the end.  The result is bit-identical to quantising the whole K and V,
+ * folding the same chunks in order and finalising.
  *   q_host, out_host   fp16 [B][n_tokens][H][64] in host memory;
  *   k_host, v_host     fp32 [B][n_tokens][H][64] in host memory;
  *                      page-locked host memory lets the copies overlap the
@@ -252,7 +255,7 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  *                      work already on the compute stream, so back-to-back calls
  *                      on the same buffers are ordered.  The output is on the
  *                      host once compute_stream has drained.
- * The call creates and releases one CUDA event; it allocates no memory.
+ * The call creates and releases two CUDA events; it allocates no memory.
  * Errors: Q8A_ERR_INVALID_ARG (sizes, null pointers), those of the calls above,
  * Q8A_ERR_CUDA (a copy, event or stream call failed).
  */

@@ -115,3 +115,25 @@ def test_burst_verification_long_context(lib):
     del v
     want = oracle_runner.attention(q.cpu().numpy(), wk8, wv8, 0.125, causal=False, q_pos0=M)
     compare(out, want, "burst 131072")
+
+
+@pytest.mark.parametrize("n_q,M,chunk", [(100, 1900, 640), (1, 1000, 1000), (128, 2000, 1024)])
+def test_paired_launch_continues_a_state(lib, n_q, M, chunk):
+    """One query tile without the causal mask runs in paired mode (the two
+    softmax pipelines take the even and odd key tiles and merge at the end).
+    Here the chunks are folded one after another into the same state, so tile
+    A starts from the state of the previous chunks; odd tile counts and a
+    ragged last chunk (1900 = 640 + 640 + 620) included."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    H = 3
+    q = seeded((1, n_q, H, 64), n_q + M, "cuda", torch.float16)
+    k, v = _kv(1, M, H, n_q + M + 1)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, n_q, q.device)
+    for s0 in range(0, M, chunk):
+        Q.attn_chunk_step(q, k8, v8, s0, min(chunk, M - s0), st, q_pos0=M, causal=False,
+                          k_offset_bytes=s0 * 68)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want, *_ = oracle_out(q, k, v, causal=False, q_pos0=M)
+    compare(out.cpu().numpy(), want, f"paired n_q{n_q} M{M} chunk{chunk}")
