@@ -11,6 +11,14 @@ diagonal), and the device holds about 0.3 GB, above the 129 MB L2.
 
   ncu --set full --clock-control none -k regex:chunk_step_kernel -s 2 -c 1 \\
       python -m chunked_prefill_attention_gb300.profile_case
+
+With --burst CONTEXT it runs Mode B burst verification instead: the 64
+candidates of the burst_m1m draw against a CONTEXT-token, 32-head Q8_0 cache
+in key ranges of --split keys (attn_chunk_step_split, paired launches), one
+warm-up call and then --reps calls.  --burst 131072 holds 0.57 GB of Q8_0 KV.
+
+  ncu --set full --clock-control none -k regex:chunk_step_kernel -s 1 -c 1 \\
+      python -m chunked_prefill_attention_gb300.profile_case --burst 131072
 """
 
 import argparse
@@ -26,8 +34,12 @@ def main(argv=None):
     p.add_argument("--chunk", type=int, default=8192)
     p.add_argument("--index", type=int, default=1)
     p.add_argument("--reps", type=int, default=2)
+    p.add_argument("--burst", type=int, default=0)
+    p.add_argument("--split", type=int, default=8192)
     a = p.parse_args(argv)
     _build.ensure_built()
+    if a.burst > 0:
+        return burst(a)
     w = W.WORKLOADS["m64k"]
     q, k, v = W.make_inputs(w, device="cuda", tokens=a.tokens)
     B, M, H, _ = q.shape
@@ -50,6 +62,39 @@ def main(argv=None):
     rows = M - (s0 // 128) * 128
     print(f"chunk {a.index} (keys {s0}..{s0 + n - 1}, query rows {s0 // 128 * 128}..{M - 1}): "
           f"{ms:.3f} ms per launch, status {rc}")
+
+
+def burst(a):
+    import torch
+
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
+
+    b = W.BURSTS["burst_m1m"]
+    q, k, v = W.make_burst_inputs(b, device="cuda", context=a.burst)
+    M = a.burst
+    k8 = Q.q8kv_quantize(k)
+    v8 = Q.q8kv_quantize(v)
+    del k, v
+    ws = torch.empty(Q.split_workspace_floats(1, b.heads, b.queries, M, a.split), dtype=torch.float32,
+                     device="cuda")
+    st = Q.State(1, b.heads, b.queries, q.device)
+
+    def call():
+        Q.attn_state_init(st)
+        Q.attn_chunk_step_split(q, k8, v8, 0, M, st, a.split, workspace=ws, q_pos0=M, causal=False)
+
+    call()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(a.reps):
+        call()
+    ev[1].record()
+    torch.cuda.synchronize()
+    rc, _ = Q.device_status()
+    ms = ev[0].elapsed_time(ev[1]) / a.reps
+    kv_bytes = 2 * b.heads * M * Q.ROW_BYTES
+    print(f"burst: {b.queries} candidates x {b.heads} heads against {M} keys, ranges of {a.split}: "
+          f"{ms:.3f} ms per call, {kv_bytes / (ms * 1e-3) / 1e9:.0f} GB/s of Q8_0 KV, status {rc}")
 
 
 if __name__ == "__main__":
