@@ -30,3 +30,23 @@ def test_pipelined_matches_device_path(lib, B, M, H, chunk):
         assert torch.equal(oh, ref.cpu())
     want, *_ = oracle_out(q, k, v)
     compare(oh.numpy(), want, f"pipelined B{B} M{M}")
+
+
+@pytest.mark.parametrize("B,M,H,chunk", [(1, 900, 2, 256), (2, 520, 3, 512)])
+def test_pipelined_without_causal_mask(lib, B, M, H, chunk):
+    """Without the causal mask every chunk updates every row, so the output is
+    finalised and copied back once at the end."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    q = seeded((B, M, H, 64), M + 81, "cuda", torch.float16)
+    k = seeded((B, M, H, 64), M + 82, "cuda")
+    v = seeded((B, M, H, 64), M + 83, "cuda")
+    ref, *_ = Q.prefill_attention(q, k, v, chunk, causal=False)
+    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    oh = torch.zeros((B, M, H, 64), dtype=torch.float16).pin_memory()
+    bufs = Q.PipelineBuffers(B, M, H, q.device)
+    Q.attn_prefill_pipelined(qh, kh, vh, oh, chunk, bufs, causal=False)
+    torch.cuda.current_stream().synchronize()
+    assert_device_clean()
+    assert torch.equal(oh, ref.cpu())
+    want, *_ = oracle_out(q, k, v, causal=False)
+    compare(oh.numpy(), want, f"pipelined non-causal B{B} M{M}")
