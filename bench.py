@@ -89,6 +89,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def quantize_record(B, M, H, D, ms, peaks, peak_src):
+    """HBM roofline of the two q8kv_quantize launches of a step (K and V):
+    fp32 read (4 B per value) plus Q8_0 written (34 B per 32 values)."""
+    n_bytes = 2 * B * M * H * (D * 4 + (D // 32) * 34)
+    gbs = n_bytes / (ms * 1e-3) / 1e9 if ms > 0 else None
+    hbm = float(peaks.get("hbm_gbs"))
+    return {"kernel": "q8kv_quantize (K and V)", "bound": "hbm", "ms_per_step": ms,
+            "algorithmic_bytes": n_bytes, "achieved": gbs, "peak": hbm, "unit": "GB/s",
+            "frac": gbs / hbm if gbs else None, "peak_kind": f"HBM copy, {peak_src}"}
+
+
 def make_record(*, value, n_gpus, steps, warmup, ms_per_step, config, extra):
     rec = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": steps,
@@ -196,9 +207,13 @@ def run_ours(args):
     chunks = [(s0, min(w.chunk, M - s0)) for s0 in range(0, M, w.chunk)]
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
+    def step(ev=None, qev=None):
+        if qev is not None:
+            qev[0].record(stream)
         Q.q8kv_quantize(k, k8, stride)
         Q.q8kv_quantize(v, v8, stride)
+        if qev is not None:
+            qev[1].record(stream)
         Q.attn_state_init(st)
         for i, (s0, n) in enumerate(chunks):
             if ev is not None:
@@ -217,6 +232,8 @@ def run_ours(args):
 
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in chunks]
            for _ in range(args.steps)]
+    qevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = None if args.no_clocks else ClockSampler(local_rank)
     dist_barrier(dist)
@@ -225,13 +242,14 @@ def run_ours(args):
         clocks.start()
     t0.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        step(evs[s], qevs[s])
     t1.record(stream)
     torch.cuda.synchronize()
     dist_barrier(dist)
     clk = clocks.stop() if clocks else None
     ms = t0.elapsed_time(t1) / args.steps
     chunk_ms = sum(a.elapsed_time(b) for per in evs for a, b in per) / args.steps
+    quant_ms = sum(a.elapsed_time(b) for a, b in qevs) / args.steps
     launches_chunk = len(chunks)
     ms_max = dist_max(dist, ms)
     rc, status = Q.device_status()
@@ -300,6 +318,7 @@ def run_ours(args):
                      "peak_kind": f"dense bf16/fp16 {peak_src} sustained (burst {peak_burst})",
                      "algorithmic": "4*D flops per unmasked (query, key) pair; %d launches/step" % launches_chunk,
                      "traffic": traffic, "traffic_note": traffic_state},
+        "quantize": quantize_record(B, M, H, D, quant_ms, peaks, peak_src),
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": n_launch,

@@ -61,3 +61,14 @@ def test_peaks_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peaks, src = bench.load_peaks()
     assert src == "fallback" and peaks["bf16_tflops"] == 1900.0
+
+
+def test_quantize_roofline_counts_fp32_in_and_q8_0_out():
+    """q8kv_quantize of K and V moves 256 B of fp32 in and 68 B of Q8_0 out per
+    64-value head row: 2 * B * M * H * 324 bytes per step."""
+    import bench
+    rec = bench.quantize_record(1, 65536, 32, 64, 0.2, {"hbm_gbs": 6795.1}, "measured")
+    assert rec["algorithmic_bytes"] == 2 * 65536 * 32 * 324
+    assert abs(rec["achieved"] - rec["algorithmic_bytes"] / 0.2e-3 / 1e9) < 1e-6
+    assert abs(rec["frac"] - rec["achieved"] / 6795.1) < 1e-12
+    assert rec["bound"] == "hbm" and rec["unit"] == "GB/s"
