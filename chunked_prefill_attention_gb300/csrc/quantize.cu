@@ -6,6 +6,15 @@
 // IEEE fp32 divide, and q = round_half_away(x / d) with an IEEE fp32 divide by
 // the stored fp16 d, clamped to [-127, 127] (d == 0 -> all codes 0).
 //
+// The quotient x / d is formed as the correctly rounded fp32 quotient without a
+// divide per value: with y = RN(1/d) (one __frcp_rn per block), q0 = RN(x*y) is
+// within one ulp of x/d, the residual r = x - q0*d is exact as one fma, and
+// RN(q0 + r*y) is RN(x/d) -- Markstein's correction theorem for division
+// with a fused multiply-add (P. Markstein, IBM J. Res. Dev. 34(1), 1990; also
+// Muller et al., "Handbook of Floating-Point Arithmetic", on fma-based
+// division).  The theorem needs a normal quotient; a quotient below 2^-126 is
+// far below 0.5 and rounds to code 0 either way.
+//
 // Memory plan (HBM-bound: 256 B read + 68 B written per 64-value head row):
 // one block handles 16 tokens x 8 heads.  Each half-warp quantises one head
 // row: its 16 lanes load the row's 256 bytes with one 128-bit load each, the 8
@@ -28,14 +37,21 @@ constexpr int kHeads = 8;   // heads per block
 constexpr int kThreads = 256;
 constexpr int kRowsPerHalfWarp = kTok * kHeads / (kThreads / 16);  // 8
 
-__device__ __forceinline__ uint32_t quant4(float4 v, float d) {
+// RN(x / d) for d > 0, from y = RN(1 / d) (see the note above).
+__device__ __forceinline__ float div_rn_by(float x, float d, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, d, x);
+  return __fmaf_rn(r, y, q0);
+}
+
+__device__ __forceinline__ uint32_t quant4(float4 v, float d, float y) {
   const float x[4] = {v.x, v.y, v.z, v.w};
   uint32_t packed = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     int q = 0;
     if (d > 0.0f) {
-      float r = roundf(__fdiv_rn(x[i], d));   // round half away from zero
+      float r = roundf(div_rn_by(x[i], d, y));   // round half away from zero
       r = fminf(fmaxf(r, -127.0f), 127.0f);
       q = static_cast<int>(r);
     }
@@ -85,7 +101,8 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
     const __half d16 = __float2half_rn(__fdiv_rn(a, 127.0f));
     const float d = __half2float(d16);
-    const uint32_t codes = quant4(v[i], d);
+    const float y = d > 0.0f ? __frcp_rn(d) : 0.0f;
+    const uint32_t codes = quant4(v[i], d, y);
     if (tok < n_tok && hh < n_h) {
       uint8_t* row = &stage[hh][tok * kRowBytes];
       const int off = 34 * blkid + 2 + 4 * (ln & 7);   // 2-byte aligned
@@ -96,15 +113,16 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   }
   __syncthreads();
 
-  // Write back: head hh's rows t0..t0+n_tok-1 are contiguous in its plane.
-  const int words_per_head = n_tok * (kRowBytes / 4);
-  const int total = n_h * words_per_head;
-  for (int w = threadIdx.x; w < total; w += kThreads) {
-    const int hh = w / words_per_head;
-    const int wi = w - hh * words_per_head;
+  // Write back: head hh's rows t0..t0+n_tok-1 are contiguous in its plane;
+  // warp hh copies them as 32-bit words.
+  static_assert(kThreads / 32 == kHeads, "one warp per head of the block");
+  const int hh = threadIdx.x >> 5;
+  if (hh < n_h) {
+    const int words = n_tok * (kRowBytes / 4);
     uint32_t* dst = reinterpret_cast<uint32_t*>(out + (b * heads + h0 + hh) * plane_stride +
                                                 t0 * kRowBytes);
-    dst[wi] = reinterpret_cast<const uint32_t*>(stage[hh])[wi];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(stage[hh]);
+    for (int wi = threadIdx.x & 31; wi < words; wi += 32) dst[wi] = src[wi];
   }
 }
 

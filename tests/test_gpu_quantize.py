@@ -49,6 +49,31 @@ def test_quantize_special_values(lib):
     _check(x, lib)
 
 
+def test_quantize_codes_next_to_half_integer_quotients(lib):
+    """Blocks whose scale is exactly d (amax = 127 d) and whose other values lie
+    within three ulps of (k + 1/2) d: the code is decided by the last bit of
+    the quotient x / d, so it must be the correctly rounded one."""
+    rng = np.random.default_rng(11)
+    M, H = 256, 16
+    x = np.empty((1, M, H, 64), dtype=np.float32)
+    for blk in range(2):
+        e = rng.integers(-12, 8, size=(M, H))
+        d = np.float16(np.ldexp(1.0 + rng.integers(0, 1024, size=(M, H)) / 1024.0, e)).astype(np.float32)
+        k = rng.integers(0, 127, size=(M, H, 31)).astype(np.float32)
+        base = ((k + 0.5) * d[..., None]).astype(np.float32)
+        ulps = rng.integers(-3, 4, size=(M, H, 31))
+        v = base.copy()
+        for step in range(3):
+            up = ulps > step
+            dn = ulps < -step
+            v = np.where(up, np.nextafter(v, np.float32(np.inf)), v)
+            v = np.where(dn, np.nextafter(v, np.float32(-np.inf)), v)
+        sign = np.where(rng.random((M, H, 31)) < 0.5, -1.0, 1.0).astype(np.float32)
+        x[0, :, :, 32 * blk] = 127.0 * d
+        x[0, :, :, 32 * blk + 1:32 * blk + 32] = v * sign
+    _check(torch.from_numpy(x).cuda(), lib)
+
+
 def test_quantize_padded_stride_leaves_padding(lib):
     from chunked_prefill_attention_gb300 import q8attn as Q
     B, M, H = 2, 7, 3
