@@ -16,7 +16,9 @@ Readings where the page is silent (each listed in the design notes):
   * amax == 0 (or a scale that underflows to fp16 zero): d16 = +0, all codes 0.
   * byte layout of one block: fp16 d (little-endian) at offset 0, then the
     32 int8 codes at offsets 2..33.  A head row of 64 values is two blocks,
-    68 bytes: channels 0..31 then 32..63.
+    68 bytes: channels 0..31 then 32..63.  A wider head row is quantised the
+    same way, one block per 32 channels in channel order (head_dim 128: four
+    blocks, 136 bytes).
 """
 
 import numpy as np
@@ -79,21 +81,26 @@ def unpack_rows(raw, nb=2):
 def quantize_kv(x):
     """Quantise a K or V tensor as the GPU path stores it.
 
-    x: float32 [B, M, H, 64] (token-major, as a projection emits it).
-    Returns uint8 [B, H, M, 68]: head-major planes of 68-byte rows.
+    x: float32 [B, M, H, D] (token-major, as a projection emits it), D a
+    multiple of 32 (64 for the GPU path).
+    Returns uint8 [B, H, M, D/32*34]: head-major planes of rows of D/32 blocks
+    (68 bytes at D = 64).
     """
     x = np.asarray(x, dtype=np.float32)
     B, M, H, D = x.shape
-    if D != 64:
-        raise ValueError("head_dim must be 64")
-    d16, q = quantize_blocks(x)                 # [B,M,H,2], [B,M,H,2,32]
-    rows = pack_rows(d16, q)                    # [B,M,H,68]
+    if D % BLOCK_VALUES or D == 0:
+        raise ValueError("head_dim must be a positive multiple of 32")
+    d16, q = quantize_blocks(x)                 # [B,M,H,D/32], [B,M,H,D/32,32]
+    rows = pack_rows(d16, q)                    # [B,M,H,D/32*34]
     return np.ascontiguousarray(rows.transpose(0, 2, 1, 3))
 
 
 def dequantize_kv(raw):
-    """uint8 [..., 68] rows -> fp64 [..., 64] exact dequantised values."""
-    d16, q = unpack_rows(raw, nb=2)
+    """uint8 [..., nb*34] rows -> fp64 [..., nb*32] exact dequantised values
+    (nb = 2 for the 68-byte rows of head_dim 64)."""
+    if raw.shape[-1] % BLOCK_BYTES:
+        raise ValueError("row length must be a multiple of 34 bytes")
+    d16, q = unpack_rows(raw, nb=raw.shape[-1] // BLOCK_BYTES)
     return dequantize_blocks(d16, q)
 
 

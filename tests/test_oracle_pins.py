@@ -158,6 +158,29 @@ def test_quantize_kv_layout_is_head_major():
     assert np.max(np.abs(y - x.transpose(0, 2, 1, 3))) <= np.max(np.abs(x)) / 127
 
 
+
+def test_quantize_kv_head_dim_128_is_four_blocks_in_channel_order():
+    """A 128-channel head row is four blocks, channels 0-31, 32-63, 64-95,
+    96-127, each quantised on its own: 136 bytes, the 34-byte block four times."""
+    rng = np.random.default_rng(16)
+    x = rng.standard_normal((1, 3, 2, 128)).astype(np.float32)
+    x[0, 1, 0, 64:96] *= 40.0       # one block with a much larger scale
+    raw = q8_0.quantize_kv(x)
+    assert raw.shape == (1, 2, 3, 136)
+    for m, h, j in itertools.product(range(3), range(2), range(4)):
+        d16, q = q8_0.quantize_blocks(x[0, m, h, 32 * j:32 * j + 32])
+        assert np.array_equal(raw[0, h, m, 34 * j:34 * j + 34], q8_0.pack_rows(d16[None], q[None])[0])
+    y = q8_0.dequantize_kv(raw)
+    assert y.shape == (1, 2, 3, 128)
+    # each block's round trip is bounded by its own scale
+    for m, h, j in itertools.product(range(3), range(2), range(4)):
+        blk = x[0, m, h, 32 * j:32 * j + 32]
+        assert np.max(np.abs(y[0, h, m, 32 * j:32 * j + 32] - blk)) <= np.max(np.abs(blk)) / 127
+    assert q8_0.kv_cache_bytes(1, 32, 1, 128) == 2 * 32 * 136
+    with pytest.raises(ValueError):
+        q8_0.quantize_kv(np.zeros((1, 1, 1, 48), dtype=np.float32))
+
+
 # ------------------------------------------------------------- attention ----
 
 def _brute(q, k, v, scale, causal=True, q_pos0=0):
@@ -179,7 +202,7 @@ def _brute(q, k, v, scale, causal=True, q_pos0=0):
 
 
 @pytest.mark.parametrize("m,d,causal,q_pos0", [(1, 4, True, 0), (3, 5, True, 0), (8, 8, True, 0),
-                                               (6, 4, False, 0), (5, 3, True, 2)])
+                                               (6, 4, False, 0), (5, 3, True, 2), (4, 128, True, 0)])
 def test_attention_matches_brute_force(m, d, causal, q_pos0):
     rng = np.random.default_rng(m * 10 + d)
     n_k = m + q_pos0
