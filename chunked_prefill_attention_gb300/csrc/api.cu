@@ -85,6 +85,7 @@ int64_t q8a_plane_stride_bytes(int64_t n_tokens) {
 
 int q8kv_quantize(const float* x, void* q8_out, int64_t batch, int64_t n_tokens, int32_t heads,
                   int32_t head_dim, int64_t out_plane_stride_bytes, void* stream) {
+  q8a::NvtxRange nvtx_range("q8kv_quantize");
   const char* fn = "q8kv_quantize";
   if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
   if (n_tokens < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_tokens must be >= 0", fn);
@@ -103,6 +104,7 @@ int q8kv_quantize(const float* x, void* q8_out, int64_t batch, int64_t n_tokens,
 
 int attn_state_init(float* m, float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
                     int32_t head_dim, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_state_init");
   const char* fn = "attn_state_init";
   if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
   if (n_q < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q must be >= 0", fn);
@@ -204,6 +206,7 @@ int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void*
                     int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
                     float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
                     float scale, int32_t causal, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_chunk_step");
   const char* fn = "attn_chunk_step";
   CUtensorMap qmap;
   q8a::ChunkArgs a;
@@ -230,6 +233,7 @@ int attn_chunk_step_gqa(const void* q, int64_t q_pos0, const void* k_q8, const v
                         int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
                         float* l, float* o, int64_t batch, int32_t heads, int32_t kv_heads,
                         int64_t n_q, int32_t head_dim, float scale, int32_t causal, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_chunk_step_gqa");
   const char* fn = "attn_chunk_step_gqa";
   if (kv_heads <= 0 || heads <= 0 || heads % kv_heads != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: heads (%d) must be a positive multiple of kv_heads (%d)",
@@ -254,6 +258,7 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
                           float* m, float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
                           int32_t head_dim, float scale, int32_t causal, int64_t split_keys,
                           float* workspace, int64_t workspace_floats, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_chunk_step_split");
   const char* fn = "attn_chunk_step_split";
   if (split_keys <= 0 || split_keys % 128 != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
@@ -340,6 +345,7 @@ int attn_chunk_step_split_static(const void* q, int64_t q_pos0, const void* k_q8
                                  float* m, float* l, float* o, int64_t batch, int32_t heads,
                                  int64_t n_q, int32_t head_dim, float scale, int32_t causal,
                                  int64_t split_keys, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_chunk_step_split_static");
   const char* fn = "attn_chunk_step_split_static";
   if (split_keys <= 0 || split_keys % 128 != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
@@ -361,6 +367,7 @@ int attn_chunk_step_split_static(const void* q, int64_t q_pos0, const void* k_q8
 
 int attn_finalize(const float* l, const float* o, void* out, int64_t batch, int32_t heads,
                   int64_t n_q, int32_t head_dim, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_finalize");
   const char* fn = "attn_finalize";
   if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
   if (n_q < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q must be >= 0", fn);

@@ -6,7 +6,19 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace q8a {
+
+// An NVTX range around one ABI call, so that Nsight tools show the library's
+// calls on the timeline; without a tool attached it does nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 
 constexpr int kHeadDim = 64;
 constexpr int kRowBytes = 68;  // one head row: two 34-byte Q8_0 blocks

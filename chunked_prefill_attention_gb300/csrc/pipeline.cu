@@ -35,6 +35,7 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
                            void* q_dev, float* k_dev, float* v_dev, void* k8, void* v8,
                            int64_t plane_stride_bytes, float* m, float* l, float* o, void* out_dev,
                            void* compute_stream, void* copy_stream) {
+  q8a::NvtxRange nvtx_range("attn_prefill_pipelined");
   if (batch < 0 || heads <= 0 || n_tokens < 0 || head_dim != Q8A_HEAD_DIM || chunk <= 0 ||
       chunk % 4 != 0)
     return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn,
