@@ -49,7 +49,9 @@
 extern "C" {
 #endif
 
-#define Q8A_ABI_VERSION 1u
+/* Raised whenever an entry point is added or its contract changes.  2: the
+ * split, allocation-free split, pipelined and grouped-query calls. */
+#define Q8A_ABI_VERSION 2u
 
 enum {
   Q8A_OK = 0,

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), f"missing export {n}"
         assert n in q8attn.SIGNATURES, f"binding lacks {n}"
-    assert lib.q8a_abi_version() == 1
+    assert lib.q8a_abi_version() == 2
 
 
 def test_plane_stride(lib):
