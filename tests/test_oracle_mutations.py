@@ -125,3 +125,42 @@ def test_attention_mutant_is_caught(name, old, new):
     except Exception:
         ok = False
     assert not ok, f"planted mistake not caught: {name}"
+
+
+def _runner_pins_pass(rm):
+    """The runner checks of test_oracle_runner.py on a mutant runner.  The
+    mutant keeps the real worker pool and task functions (spawned workers can
+    only import the real module); every planted slip below sits in the code that
+    runs in this process."""
+    from oracle import runner
+    from tests import test_oracle_runner as pins
+    rm.pool, rm._attn_task, rm._quant_task = runner.pool, runner._attn_task, runner._quant_task
+    return (pins.runner_attention_agrees(rm, H_kv=2, causal=True)
+            and pins.runner_attention_agrees(rm, H_kv=1, causal=False)
+            and pins.runner_quantize_agrees(rm))
+
+
+RUNNER_MUTANTS = [
+    ("plane assembly swaps batch and head", "out[i // H, :, i % H] = r", "out[i % B, :, i // B] = r"),
+    ("interleaved head groups", "g = h // group", "g = h % H_kv"),
+    ("quantise pieces joined in reverse token order",
+     "parts.append(np.concatenate(pool().map(_quant_task, tasks), axis=2))",
+     "parts.append(np.concatenate(pool().map(_quant_task, tasks)[::-1], axis=2))"),
+    ("quantise batch entries swapped", "return np.concatenate(parts, axis=0)",
+     "return np.concatenate(parts[::-1], axis=0)"),
+    ("causal key range cut one short",
+     "min(k8.shape[2], q_pos0 + int(rows.max()) + 1)", "min(k8.shape[2], q_pos0 + int(rows.max()))"),
+]
+
+
+def test_unmutated_runner_passes_the_checks():
+    assert _runner_pins_pass(_mutant("runner", "", ""))
+
+
+@pytest.mark.parametrize("name,old,new", RUNNER_MUTANTS, ids=[m[0] for m in RUNNER_MUTANTS])
+def test_runner_mutant_is_caught(name, old, new):
+    try:
+        ok = _runner_pins_pass(_mutant("runner", old, new))
+    except Exception:
+        ok = False
+    assert not ok, f"planted mistake not caught: {name}"
