@@ -48,6 +48,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
+    p.add_argument("--other-workloads", default="m512,m2k_out,b8_m2k,m1m",
+                   help="comma-separated workloads also timed (one GPU only) and reported under "
+                        "'workloads'; empty to skip")
     return p.parse_args(argv)
 
 
@@ -185,6 +188,100 @@ def profile_traffic(kernel_src):
         return None, "absent"
 
 
+def step_hbm_bytes(w):
+    """Algorithmic HBM bytes of one step of workload w: quantise K and V (256 B
+    fp32 in + 68 B Q8_0 out per head row each), state init (264 B per state
+    row), one chunk step per KV chunk (per state row it touches: 128 B of Q and
+    2 x 264 B of state; per chunk key and head: 136 B of Q8_0 K and V), finalise
+    (260 B in + 128 B out per state row)."""
+    B, M, H = w.batch, w.tokens, w.heads
+    rows = B * H * M
+    total = 2 * rows * 324 + rows * 264 + rows * 388
+    for s0 in range(0, M, w.chunk):
+        n = min(w.chunk, M - s0)
+        total += B * H * (M - s0) * (128 + 528) + B * H * n * 136
+    return total
+
+
+def time_workload(name, steps, warmup, peaks, peak_src, flush_l2, sample_clocks):
+    """Time the whole step of another workload on the current device: each
+    step bracketed by its own CUDA events (and, for problems smaller than L2,
+    preceded by a write of a 256 MB buffer outside the events).  Returns its
+    record for the 'workloads' key."""
+    import torch
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
+    w = W.WORKLOADS[name]
+    dev = torch.cuda.current_device()
+    B, M, H, D = w.batch, w.tokens, w.heads, w.head_dim
+    q, k, v = W.make_inputs(w, device=torch.device("cuda", dev))
+    stride = Q.plane_stride(M)
+    k8 = torch.empty((B, H, stride), dtype=torch.uint8, device=q.device)
+    v8 = torch.empty((B, H, stride), dtype=torch.uint8, device=q.device)
+    st = Q.State(B, H, M, q.device, init=False)
+    out = torch.empty((B, M, H, D), dtype=torch.float16, device=q.device)
+    chunks = [(s0, min(w.chunk, M - s0)) for s0 in range(0, M, w.chunk)]
+    stream = torch.cuda.current_stream()
+    scratch = torch.empty((256 << 20,), dtype=torch.uint8, device=q.device) if flush_l2 else None
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        Q.q8kv_quantize(k, k8, stride)
+        Q.q8kv_quantize(v, v8, stride)
+        Q.attn_state_init(st)
+        if ev is not None:
+            ev[1].record(stream)
+        for s0, n in chunks:
+            Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * 68)
+        if ev is not None:
+            ev[2].record(stream)
+        Q.attn_finalize(st, out)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    clocks = ClockSampler(dev) if sample_clocks else None
+    if clocks:
+        clocks.start()
+    for s in range(steps):
+        if scratch is not None:
+            scratch.zero_()
+        step(evs[s])
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    rc, status = Q.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {status:#x} after timing {name}")
+    ms = sum(e[0].elapsed_time(e[3]) for e in evs) / steps
+    chunk_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    tflops = w.causal_flops / (ms * 1e-3) / 1e12
+    rec = {"workload": w.describe(), "ms_per_step": ms, "tflops": tflops,
+           "tokens_per_s": B * M / (ms * 1e-3), "steps": steps, "warmup": warmup,
+           "l2": ("L2 flushed before each step (256 MB write outside the timed events)" if flush_l2
+                  else "inputs larger than L2")}
+    if w.tokens >= 65536:
+        peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+        achieved = w.causal_flops / (chunk_ms * 1e-3) / 1e12
+        rec["roofline"] = {"bound": "tensor", "kernel": "attn_chunk_step", "achieved": achieved,
+                           "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                           "peak_kind": f"dense bf16/fp16 {peak_src} sustained",
+                           "ms_attn_chunks_per_step": chunk_ms}
+    else:
+        hbm = float(peaks.get("hbm_gbs"))
+        n_bytes = step_hbm_bytes(w)
+        gbs = n_bytes / (ms * 1e-3) / 1e9
+        rec["roofline"] = {"bound": "hbm", "kernel": "whole step (%d launches)" % (4 + len(chunks)),
+                           "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                           "algorithmic_bytes": n_bytes, "peak_kind": f"HBM copy, {peak_src}"}
+    rec["clocks"] = clk
+    del q, k, v, k8, v8, st, out, scratch
+    torch.cuda.empty_cache()
+    return rec
+
+
 # ------------------------------------------------------------------ our arm --
 
 def run_ours(args):
@@ -276,11 +373,11 @@ def run_ours(args):
         kh = k.cpu().pin_memory()
         vh = v.cpu().pin_memory()
         oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        bufs = Q.PipelineBuffers(B, M, H, dev)
+        bufs = Q.PipelineBuffers(B, M, H, dev, w.chunk)
 
         def e2e_step():
             # attn_prefill_pipelined: K/V chunk copies overlap quantise + chunk steps
-            Q.attn_prefill_pipelined(qh, kh, vh, oh, w.chunk, bufs)
+            Q.attn_prefill_pipelined(qh, kh, vh, oh, bufs)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -301,12 +398,24 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, q, k, v, budget_s=30.0)
 
+    others = {}
+    names = [n for n in args.other_workloads.split(",") if n and n != w.name]
+    if world == 1 and names:
+        bufs = None
+        del q, k, v, k8, v8, out
+        torch.cuda.empty_cache()
+        for name in names:
+            big = W.WORKLOADS[name].tokens >= 1 << 20
+            others[name] = time_workload(name, 2 if big else 20, 1 if big else 3, peaks, peak_src,
+                                         flush_l2=W.WORKLOADS[name].tokens < 65536,
+                                         sample_clocks=big and not args.no_clocks)
+
     n_launch = args.steps * (3 + len(chunks) + 1)
     config = {
         "workload": w.describe(), "batch": B, "tokens": M, "heads": H, "head_dim": D,
         "kv_chunk": w.chunk, "kv_chunks": len(chunks), "replicas": world,
         "l2": "inputs larger than L2: K, V fp32 %.2f GB, Q fp16 %.2f GB, Q8_0 KV %.2f GB, state %.2f GB"
-              % (2 * k.nbytes / 1e9, q.nbytes / 1e9, 2 * B * H * stride / 1e9,
+              % (2 * B * M * H * D * 4 / 1e9, B * M * H * D * 2 / 1e9, 2 * B * H * stride / 1e9,
                  (st.m.nbytes + st.l.nbytes + st.o.nbytes) / 1e9),
     }
     extra = {
@@ -323,6 +432,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": n_launch,
         "cpu_baseline": cpu,
+        "workloads": others or None,
     }
     rec = make_record(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                       ms_per_step=ms_max, config=config, extra=extra)

@@ -28,8 +28,13 @@ int ok() {
   g_err[0] = '\0';
   return Q8A_OK;
 }
+thread_local char g_note[256] = "";
+
 int cuda_fail(cudaError_t e, const char* what) {
-  return fail(Q8A_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  const int rc = fail(Q8A_ERR_CUDA, "%s: %s (%s)%s%s", what, cudaGetErrorName(e), cudaGetErrorString(e),
+                      g_note[0] ? ": " : "", g_note);
+  g_note[0] = '\0';
+  return rc;
 }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -59,6 +64,15 @@ EncodeTiledFn encode_fn() {
 
 int q8a::set_error(int code, const char* fn, const char* msg) {
   return fail(code, "%s: %s", fn, msg);
+}
+
+const char* q8a::launch_note() { return g_note; }
+
+void q8a::set_launch_note(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_note, sizeof(g_note), fmt, ap);
+  va_end(ap);
 }
 
 namespace {
@@ -303,10 +317,12 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
 
 // ---- allocation-free split step ----------------------------------------------
 // Scratch for attn_chunk_step_split_static: the partial states live in this
-// fixed array, which every GPU that loads the library holds until the process
-// exits.  In host code the symbol is only a stand-in; its device address is
-// fetched once per device (with that device current) and handed to the
-// kernels like any workspace.
+// fixed array, which takes 32 MiB on each GPU where the library's kernels are
+// loaded (under lazy module loading, the GPUs where one of them first runs)
+// until the process exits.  In host code the symbol is only a stand-in; its
+// device address is looked up once per device with that device current, and
+// again whenever the device's current context has changed (after a device
+// reset the module is loaded anew and the array may sit elsewhere).
 namespace {
 
 constexpr int64_t kStaticSplitFloats = 8ll * 1024 * 1024;   // 32 MiB
@@ -315,20 +331,43 @@ __device__ __align__(256) float g_static_split_scratch[kStaticSplitFloats];
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;
 float* g_static_ptr[kMaxDevices] = {};
+CUcontext g_static_ctx[kMaxDevices] = {};
 
-// Device address of the scratch on the current device (looked up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of the scratch on the current device.
 int static_scratch(const char* fn, float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   if (dev < 0 || dev >= kMaxDevices)
     return fail(Q8A_ERR_UNSUPPORTED, "%s: device ordinal %d beyond %d", fn, dev, kMaxDevices);
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx) return fail(Q8A_ERR_CUDA, "%s: cuCtxGetCurrent unavailable", fn);
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (!g_static_ptr[dev]) {
+  if (!ctx || !g_static_ptr[dev] || g_static_ctx[dev] != ctx) {
+    // the lookup itself makes the device's primary context current
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_split_scratch);
     if (e != cudaSuccess) return cuda_fail(e, fn);
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return fail(Q8A_ERR_CUDA, "%s: no current CUDA context", fn);
     g_static_ptr[dev] = static_cast<float*>(p);
+    g_static_ctx[dev] = ctx;
   }
   *out = g_static_ptr[dev];
   return Q8A_OK;

@@ -80,6 +80,11 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
 // Record `msg` as the calling thread's last error (q8a_last_error) and return code.
 int set_error(int code, const char* fn, const char* msg);
 
+// A launcher that refuses a launch configuration describes why here (thread
+// local; "" when the last refusal had no note).
+const char* launch_note();
+void set_launch_note(const char* fmt, ...);
+
 // Merge the n_splits partial states of a split chunk step into (m, l, o).
 cudaError_t launch_split_merge(const ChunkArgs& args, cudaStream_t stream);
 

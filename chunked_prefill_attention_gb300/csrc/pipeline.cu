@@ -3,12 +3,16 @@
 // it.
 //
 // This is the GB300 form of the pages' out-of-core streaming ("Out-of-Core
-// Flash Streaming & Speculative Decode (1M Context)", §2: while the GPU folds
-// chunk c into the persistent state, the next chunk is already being read into
-// a second buffer).  Here the source is pinned host memory instead of flash,
-// the copies run on a copy stream, and each chunk's Q8_0 quantisation and
-// chunk step wait on that chunk's copy through an event.  Host code only: every
-// step of the computation is one of the library's kernels.
+// Flash Streaming & Speculative Decode (1M Context)", §2 "Double-Buffered
+// Ping-Pong Execution": while the GPU folds chunk c into the persistent state,
+// the next chunk is already being read into the second of two fixed slots).
+// Here the source is pinned host memory instead of flash, the copies run on a
+// copy stream into two device slots of one chunk's fp32 K and V each (so the
+// fp32 inputs take device memory in proportion to the chunk, not the
+// sequence), and each chunk's Q8_0 quantisation and chunk step wait on that
+// chunk's copy through an event; a slot is refilled only after the quantise
+// that read it.  Host code only: every step of the computation is one of the
+// library's kernels.
 
 #include <cstdio>
 
@@ -29,10 +33,15 @@ int cuda_err(cudaError_t e, const char* what) {
 
 extern "C" {
 
+int64_t q8a_prefill_slot_floats(int64_t batch, int32_t heads, int64_t chunk) {
+  if (batch < 0 || heads <= 0 || chunk <= 0) return -1;
+  return 4 * batch * chunk * heads * Q8A_HEAD_DIM;   // 2 slots x (K, V) x [B][chunk][H][64]
+}
+
 int attn_prefill_pipelined(const void* q_host, const float* k_host, const float* v_host,
                            void* out_host, int64_t batch, int32_t heads, int64_t n_tokens,
                            int32_t head_dim, int64_t chunk, float scale, int32_t causal,
-                           void* q_dev, float* k_dev, float* v_dev, void* k8, void* v8,
+                           void* q_dev, float* kv_slots, int64_t kv_slot_floats, void* k8, void* v8,
                            int64_t plane_stride_bytes, float* m, float* l, float* o, void* out_dev,
                            void* compute_stream, void* copy_stream) {
   q8a::NvtxRange nvtx_range("attn_prefill_pipelined");
@@ -42,28 +51,45 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
                           "sizes must be >= 0, heads > 0, head_dim 64 and chunk a positive "
                           "multiple of 4");
   if (batch == 0 || n_tokens == 0) return Q8A_OK;
-  if (!q_host || !k_host || !v_host || !out_host || !q_dev || !k_dev || !v_dev || !k8 || !v8 ||
-      !m || !l || !o || !out_dev)
+  if (!q_host || !k_host || !v_host || !out_host || !q_dev || !kv_slots || !k8 || !v8 || !m ||
+      !l || !o || !out_dev)
     return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn, "null pointer");
+  // a chunk longer than the sequence only needs the sequence's tokens in a slot
+  const int64_t slot_tokens = chunk < n_tokens ? chunk : n_tokens;
+  if (kv_slot_floats < q8a_prefill_slot_floats(batch, heads, slot_tokens))
+    return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn,
+                          "kv_slots holds fewer than q8a_prefill_slot_floats(batch, heads, "
+                          "min(chunk, n_tokens)) floats");
+  if (reinterpret_cast<uintptr_t>(kv_slots) % 16 != 0)
+    return q8a::set_error(Q8A_ERR_MISALIGNED, kFn, "kv_slots needs 16-byte alignment");
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
   cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
   const int64_t row_floats = static_cast<int64_t>(heads) * Q8A_HEAD_DIM;   // one token, all heads
   const size_t q_bytes = static_cast<size_t>(batch * n_tokens * row_floats) * 2;
+  // slot s holds K at kv_slots + 2*s*part and V at kv_slots + (2*s+1)*part, each
+  // [B][slot_tokens][H][64] (a shorter last chunk keeps the per-sequence stride)
+  const int64_t part = batch * slot_tokens * row_floats;
 
   // ev: a chunk's inputs are on the device (copy stream -> compute stream);
-  // ev_fin: a row block of the output is final (compute stream -> copy stream).
-  cudaEvent_t ev = nullptr, ev_fin = nullptr;
-  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-  if (e != cudaSuccess) return cuda_err(e, "cudaEventCreateWithFlags");
-  e = cudaEventCreateWithFlags(&ev_fin, cudaEventDisableTiming);
-  if (e != cudaSuccess) {
-    cudaEventDestroy(ev);
-    return cuda_err(e, "cudaEventCreateWithFlags");
+  // ev_fin: a row block of the output is final (compute stream -> copy stream);
+  // ev_free[s]: slot s has been quantised and may be refilled (compute -> copy).
+  cudaEvent_t ev = nullptr, ev_fin = nullptr, ev_free[2] = {nullptr, nullptr};
+  cudaEvent_t* all[4] = {&ev, &ev_fin, &ev_free[0], &ev_free[1]};
+  auto release = [&]() {
+    for (cudaEvent_t* p : all)   // released once the recorded work is done
+      if (*p) cudaEventDestroy(*p);
+  };
+  for (cudaEvent_t* p : all) {
+    cudaError_t ce = cudaEventCreateWithFlags(p, cudaEventDisableTiming);
+    if (ce != cudaSuccess) {
+      release();
+      return cuda_err(ce, "cudaEventCreateWithFlags");
+    }
   }
+  cudaError_t e = cudaSuccess;
   int rc = Q8A_OK;
   auto bail = [&](int code) {
-    cudaEventDestroy(ev);   // released once the recorded work is done
-    cudaEventDestroy(ev_fin);
+    release();
     return code;
   };
   const size_t out_row_bytes = static_cast<size_t>(row_floats) * 2;   // one token, all heads, fp16
@@ -92,13 +118,21 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
   // and copied back on the copy stream behind the next chunk's inputs, while
   // the device works on the chunks after it.
   int64_t prev_r0 = -1, prev_n = 0;   // row block finalised but not yet copied back
-  for (int64_t s0 = 0; s0 < n_tokens; s0 += chunk) {
+  int64_t c = 0;                      // chunk index; chunk c uses slot c % 2
+  for (int64_t s0 = 0; s0 < n_tokens; s0 += chunk, ++c) {
     const int64_t n = (n_tokens - s0 < chunk) ? n_tokens - s0 : chunk;
+    const int slot = static_cast<int>(c & 1);
+    float* ks = kv_slots + 2 * slot * part;
+    float* vs = ks + part;
     const size_t bytes = static_cast<size_t>(n * row_floats) * sizeof(float);
+    // the slot's previous chunk (c - 2) must have been quantised before it is refilled
+    if (c >= 2 && (e = cudaStreamWaitEvent(xs, ev_free[slot], 0)) != cudaSuccess)
+      return bail(cuda_err(e, "cudaStreamWaitEvent"));
     for (int64_t b = 0; b < batch; ++b) {
-      const int64_t off = (b * n_tokens + s0) * row_floats;
-      if ((e = cudaMemcpyAsync(k_dev + off, k_host + off, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
-          (e = cudaMemcpyAsync(v_dev + off, v_host + off, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+      const int64_t src = (b * n_tokens + s0) * row_floats;
+      const int64_t dst = b * slot_tokens * row_floats;
+      if ((e = cudaMemcpyAsync(ks + dst, k_host + src, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(vs + dst, v_host + src, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
         return bail(cuda_err(e, "copy of a K/V chunk"));
     }
     // the chunk (and, before it on the copy stream, Q) is on the device once ev fires
@@ -111,13 +145,14 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
     }
     if ((e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
     for (int64_t b = 0; b < batch; ++b) {
-      const int64_t off = (b * n_tokens + s0) * row_floats;
+      const int64_t off = b * slot_tokens * row_floats;
       uint8_t* kq = static_cast<uint8_t*>(k8) + b * heads * plane_stride_bytes + s0 * Q8A_ROW_BYTES;
       uint8_t* vq = static_cast<uint8_t*>(v8) + b * heads * plane_stride_bytes + s0 * Q8A_ROW_BYTES;
-      if ((rc = q8kv_quantize(k_dev + off, kq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK ||
-          (rc = q8kv_quantize(v_dev + off, vq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK)
+      if ((rc = q8kv_quantize(ks + off, kq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK ||
+          (rc = q8kv_quantize(vs + off, vq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK)
         return bail(rc);
     }
+    if ((e = cudaEventRecord(ev_free[slot], cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
     if ((rc = attn_chunk_step(q_dev, 0, static_cast<const uint8_t*>(k8) + s0 * Q8A_ROW_BYTES,
                               static_cast<const uint8_t*>(v8) + s0 * Q8A_ROW_BYTES, plane_stride_bytes,
                               s0, n, m, l, o, batch, heads, n_tokens, head_dim, scale, causal, cs)) != Q8A_OK)
@@ -139,6 +174,8 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
     if ((e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
     return bail(Q8A_OK);
   }
+  // without the mask: the copy stream's last work (the slot copies) is done
+  // before the compute stream's quantise of them, so nothing else to wait for
   if ((rc = attn_finalize(l, o, out_dev, batch, heads, n_tokens, head_dim, cs)) != Q8A_OK) return bail(rc);
   if ((e = copy_out_rows(0, n_tokens, cs)) != cudaSuccess) return bail(cuda_err(e, "copy of the output"));
   return bail(Q8A_OK);

@@ -16,12 +16,15 @@
 // far below 0.5 and rounds to code 0 either way.
 //
 // Memory plan (HBM-bound: 256 B read + 68 B written per 64-value head row):
-// one block handles 16 tokens x 8 heads.  Each half-warp quantises one head
-// row: its 16 lanes load the row's 256 bytes with one 128-bit load each, the 8
-// lanes of a 32-value block reduce amax with three xor-shuffles, and every lane
-// emits 4 codes.  Rows are assembled in shared memory so that each head's 16
-// consecutive output rows (1088 contiguous bytes of the head-major plane) are
-// written back as coalesced 32-bit words.
+// one block handles 16 tokens x 8 heads, one warp per head and one thread per
+// 32-value block (lane 2t + j: token t, block j).  A thread loads its block's
+// 128 contiguous bytes with four 256-bit loads (eight 128-bit loads when x is
+// only 16-byte aligned), reduces amax in registers, forms d and the reciprocal
+// once, and emits its 32 codes as eight 32-bit words into its head's staging
+// rows in shared memory.  The warp then writes its head's 16 consecutive rows
+// (1088 contiguous, 16-byte-aligned bytes of the head-major plane) back with
+// 128-bit stores (32-bit stores for a ragged last tile); no block-wide barrier,
+// so the warps of a block load, convert and store independently.
 // This translation unit must not be built with fast-math (IEEE divides).
 
 #include <cuda_fp16.h>
@@ -34,8 +37,8 @@ namespace {
 
 constexpr int kTok = 16;    // tokens per block
 constexpr int kHeads = 8;   // heads per block
-constexpr int kThreads = 256;
-constexpr int kRowsPerHalfWarp = kTok * kHeads / (kThreads / 16);  // 8
+constexpr int kThreads = 256;   // two per head row
+static_assert(kThreads == 2 * kTok * kHeads, "one thread per 32-value block");
 
 // RN(x / d) for d > 0, from y = RN(1 / d) (see the note above).
 __device__ __forceinline__ float div_rn_by(float x, float d, float y) {
@@ -44,22 +47,27 @@ __device__ __forceinline__ float div_rn_by(float x, float d, float y) {
   return __fmaf_rn(r, y, q0);
 }
 
-__device__ __forceinline__ uint32_t quant4(float4 v, float d, float y) {
-  const float x[4] = {v.x, v.y, v.z, v.w};
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int q = 0;
-    if (d > 0.0f) {
-      float r = roundf(div_rn_by(x[i], d, y));   // round half away from zero
-      r = fminf(fmaxf(r, -127.0f), 127.0f);
-      q = static_cast<int>(r);
-    }
-    packed |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
-  }
-  return packed;
+// One code: round half away from zero of x / d, clamped to [-127, 127].  With
+// a finite d = 0 every code is 0; so is every code of a block whose scale
+// rounded to +inf in fp16 (amax beyond 65504 * 127), where x / inf = 0.
+__device__ __forceinline__ uint32_t code8(float x, float d, float y, bool finite_nonzero) {
+  if (!finite_nonzero) return 0u;
+  float r = roundf(div_rn_by(x, d, y));
+  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  return static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu;
 }
 
+// 256-bit read-only load of eight consecutive floats (32-byte aligned).
+__device__ __forceinline__ void ldg256(const float* p, float* v) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
+// kWide: x is 32-byte aligned and every block is loaded with 256-bit loads
+// (every block starts a multiple of 128 bytes after x); otherwise 128-bit loads.
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads)
 q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t n_tokens,
                      int32_t heads, int64_t plane_stride, int32_t tok_tiles, int32_t head_tiles) {
@@ -75,54 +83,75 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   const int n_tok = static_cast<int>(i64min(kTok, n_tokens - t0));
   const int n_h = min(kHeads, heads - h0);
 
-  const int hw = threadIdx.x >> 4;   // half-warp: one head row at a time
-  const int ln = threadIdx.x & 15;   // lane in half-warp: 4 consecutive channels
-  const int blkid = ln >> 3;         // 32-value block of the row (0 or 1)
-
-  // Issue all loads first: rows hw, hw+16, ... (row rr -> token rr/8, head rr%8)
-  float4 v[kRowsPerHalfWarp];
+  // warp -> head hh of the tile; lane -> (token tok, 32-value block bb)
+  const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (hh >= n_h) return;
+  const int tok = lane >> 1, bb = lane & 1;
+  const bool valid = tok < n_tok;
+  float v[32];
+  if (valid) {
+    const float* src = x + (((b * n_tokens + t0 + tok) * heads + h0 + hh) * kHeadDim + 32 * bb);
+    if (kWide) {
 #pragma unroll
-  for (int i = 0; i < kRowsPerHalfWarp; ++i) {
-    const int rr = hw + 16 * i;
-    const int tok = rr >> 3, hh = rr & 7;
-    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (tok < n_tok && hh < n_h) {
-      const float* src = x + (((b * n_tokens + t0 + tok) * heads + h0 + hh) * kHeadDim + 4 * ln);
-      v[i] = __ldg(reinterpret_cast<const float4*>(src));
+      for (int i = 0; i < 4; ++i) ldg256(src + 8 * i, v + 8 * i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(src) + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+  }
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
+  const __half d16 = __float2half_rn(__fdiv_rn(a, 127.0f));
+  const float d = __half2float(d16);
+  const bool finite_nonzero = d > 0.0f && d <= 65504.0f;
+  const float y = finite_nonzero ? __frcp_rn(d) : 0.0f;
+  uint32_t w[8];   // codes 4k .. 4k+3, little-endian
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    w[k] = code8(v[4 * k], d, y, finite_nonzero) | (code8(v[4 * k + 1], d, y, finite_nonzero) << 8) |
+           (code8(v[4 * k + 2], d, y, finite_nonzero) << 16) |
+           (code8(v[4 * k + 3], d, y, finite_nonzero) << 24);
+  const uint32_t dbits = __half_as_ushort(d16);
+  if (valid) {
+    // row bytes: block 0 = d at 0, codes at 2..33; block 1 = d at 34, codes at 36..67
+    uint8_t* row = &stage[hh][tok * kRowBytes];   // 4-byte aligned (68-byte rows)
+    if (bb == 0) {
+      uint32_t* p = reinterpret_cast<uint32_t*>(row);
+      p[0] = dbits | (w[0] << 16);
+#pragma unroll
+      for (int k = 0; k < 7; ++k) p[1 + k] = __funnelshift_r(w[k], w[k + 1], 16);
+      *reinterpret_cast<uint16_t*>(row + 32) = static_cast<uint16_t>(w[7] >> 16);
+    } else {
+      *reinterpret_cast<uint16_t*>(row + 34) = static_cast<uint16_t>(dbits);
+      uint32_t* p = reinterpret_cast<uint32_t*>(row + 36);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) p[k] = w[k];
     }
   }
-#pragma unroll
-  for (int i = 0; i < kRowsPerHalfWarp; ++i) {
-    const int rr = hw + 16 * i;
-    const int tok = rr >> 3, hh = rr & 7;
-    float a = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
-    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-    const __half d16 = __float2half_rn(__fdiv_rn(a, 127.0f));
-    const float d = __half2float(d16);
-    const float y = d > 0.0f ? __frcp_rn(d) : 0.0f;
-    const uint32_t codes = quant4(v[i], d, y);
-    if (tok < n_tok && hh < n_h) {
-      uint8_t* row = &stage[hh][tok * kRowBytes];
-      const int off = 34 * blkid + 2 + 4 * (ln & 7);   // 2-byte aligned
-      *reinterpret_cast<uint16_t*>(row + off) = static_cast<uint16_t>(codes & 0xFFFFu);
-      *reinterpret_cast<uint16_t*>(row + off + 2) = static_cast<uint16_t>(codes >> 16);
-      if ((ln & 7) == 0) *reinterpret_cast<__half*>(row + 34 * blkid) = d16;
-    }
-  }
-  __syncthreads();
+  __syncwarp();
 
-  // Write back: head hh's rows t0..t0+n_tok-1 are contiguous in its plane;
-  // warp hh copies them as 32-bit words.
-  static_assert(kThreads / 32 == kHeads, "one warp per head of the block");
-  const int hh = threadIdx.x >> 5;
-  if (hh < n_h) {
-    const int words = n_tok * (kRowBytes / 4);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(out + (b * heads + h0 + hh) * plane_stride +
-                                                t0 * kRowBytes);
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(stage[hh]);
-    for (int wi = threadIdx.x & 31; wi < words; wi += 32) dst[wi] = src[wi];
+  // Write back: head hh's rows t0 .. t0+n_tok-1 are contiguous in its plane
+  // (byte t0 * 68 = tt * 1088, a multiple of 16).
+  static_assert(kThreads / 32 == kHeads && 2 * kTok == 32, "one warp per head, two lanes per token");
+  uint8_t* dst = out + (b * heads + h0 + hh) * plane_stride + t0 * kRowBytes;
+  if (n_tok == kTok) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(stage[hh]);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int i = lane; i < kTok * kRowBytes / 16; i += 32) d4[i] = s4[i];
+  } else {
+    const uint32_t* s1 = reinterpret_cast<const uint32_t*>(stage[hh]);
+    uint32_t* d1 = reinterpret_cast<uint32_t*>(dst);
+    for (int i = lane; i < n_tok * (kRowBytes / 4); i += 32) d1[i] = s1[i];
   }
 }
 
@@ -135,7 +164,9 @@ cudaError_t launch_quantize(const float* x, uint8_t* out, int64_t batch, int64_t
   const int64_t blocks = batch * tok_tiles * head_tiles;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF || tok_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  q8kv_quantize_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+  const bool wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0;
+  auto kernel = wide ? q8kv_quantize_kernel<true> : q8kv_quantize_kernel<false>;
+  kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
       x, out, n_tokens, heads, plane_stride, static_cast<int32_t>(tok_tiles),
       static_cast<int32_t>(head_tiles));
   return cudaGetLastError();

@@ -46,7 +46,8 @@ SIGNATURES = {
     "q8a_static_split_scratch_floats": (_I64, []),
     "attn_finalize": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
     "attn_prefill_pipelined": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, _I64, _I32, _I64, _F, _I32,
-                                              _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
+                                              _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
+    "q8a_prefill_slot_floats": (_I64, [_I64, _I32, _I64]),
     "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
     "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),
     "q8a_test_inject": (ctypes.c_int, [_I32]),
@@ -227,14 +228,19 @@ def prefill_attention(q, k, v, chunk, scale=None, causal=True, k8=None, v8=None,
 
 
 class PipelineBuffers:
-    """Device buffers of attn_prefill_pipelined for one problem size."""
+    """Device buffers of attn_prefill_pipelined for one problem size and chunk:
+    Q and the output (whole sequence), two chunk slots of fp32 K and V, the
+    Q8_0 planes of the whole sequence and the state."""
 
-    def __init__(self, batch, n_tokens, heads, device):
+    def __init__(self, batch, n_tokens, heads, device, chunk):
         shape = (batch, n_tokens, heads, HEAD_DIM)
+        self.chunk = chunk
         self.q = torch.empty(shape, dtype=torch.float16, device=device)
-        self.k = torch.empty(shape, dtype=torch.float32, device=device)
-        self.v = torch.empty(shape, dtype=torch.float32, device=device)
         self.out = torch.empty(shape, dtype=torch.float16, device=device)
+        n_slot = int(load().q8a_prefill_slot_floats(batch, heads, min(chunk, n_tokens)))
+        if n_slot < 0:
+            raise Q8AttnError(Q8A_ERR_INVALID_ARG, "invalid sizes for the prefill slots")
+        self.kv_slots = torch.empty((n_slot,), dtype=torch.float32, device=device)
         self.stride = plane_stride(n_tokens)
         self.k8 = torch.empty((batch, heads, self.stride), dtype=torch.uint8, device=device)
         self.v8 = torch.empty((batch, heads, self.stride), dtype=torch.uint8, device=device)
@@ -242,19 +248,20 @@ class PipelineBuffers:
         self.copy_stream = torch.cuda.Stream(device=device)
 
 
-def attn_prefill_pipelined(q_host, k_host, v_host, out_host, chunk, bufs, scale=None, causal=True):
-    """The whole prefill from host tensors (page-locked for overlap): K/V chunk
-    copies on bufs.copy_stream overlap quantise + chunk step on the current
-    stream; the output lands in out_host once the current stream drains."""
+def attn_prefill_pipelined(q_host, k_host, v_host, out_host, bufs, scale=None, causal=True):
+    """The whole prefill from host tensors (page-locked for overlap) in chunks of
+    bufs.chunk tokens: K/V chunk copies on bufs.copy_stream into two device
+    slots overlap quantise + chunk step on the current stream; the output lands
+    in out_host once the current stream drains."""
     B, M, H, D = q_host.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     st = bufs.state
     _check(load().attn_prefill_pipelined(
-        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), B, H, M, D, chunk, scale,
-        int(bool(causal)), _ptr(bufs.q), _ptr(bufs.k), _ptr(bufs.v), _ptr(bufs.k8), _ptr(bufs.v8),
-        bufs.stride, _ptr(st.m), _ptr(st.l), _ptr(st.o), _ptr(bufs.out), _stream(bufs.q),
-        ctypes.c_void_p(bufs.copy_stream.cuda_stream)))
+        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), B, H, M, D, bufs.chunk, scale,
+        int(bool(causal)), _ptr(bufs.q), _ptr(bufs.kv_slots), bufs.kv_slots.numel(), _ptr(bufs.k8),
+        _ptr(bufs.v8), bufs.stride, _ptr(st.m), _ptr(st.l), _ptr(st.o), _ptr(bufs.out),
+        _stream(bufs.q), ctypes.c_void_p(bufs.copy_stream.cuda_stream)))
     return out_host
 
 

@@ -50,8 +50,9 @@ extern "C" {
 #endif
 
 /* Raised whenever an entry point is added or its contract changes.  2: the
- * split, allocation-free split, pipelined and grouped-query calls. */
-#define Q8A_ABI_VERSION 2u
+ * split, allocation-free split, pipelined and grouped-query calls.  3: the
+ * pipelined call streams K and V through two chunk slots (kv_slots). */
+#define Q8A_ABI_VERSION 3u
 
 enum {
   Q8A_OK = 0,
@@ -179,6 +180,10 @@ int attn_chunk_step_gqa(const void *q, int64_t q_pos0, const void *k_q8, const v
  * Two kernel launches on `stream`.  Errors: as attn_chunk_step; Q8A_ERR_INVALID_ARG
  * also for a bad split_keys or a missing or too small workspace;
  * Q8A_ERR_UNSUPPORTED beyond 65,535 key ranges.
+ * If q8a_device_status later reports Q8A_ERR_TIMEOUT for work that includes
+ * this call, some key ranges may not have written their partial states and the
+ * merge may have folded stale workspace contents into (m, l, O): the state is
+ * then undefined and must be re-initialised with attn_state_init.
  */
 int attn_chunk_step_split(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,
                           int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
@@ -199,20 +204,26 @@ int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, in
  * other allocations, or a latency-critical loop that cannot afford the
  * implicit device synchronisation of cudaMalloc / cudaFree.  It allocates
  * nothing: the partial states live in a fixed scratch array inside the
- * library (q8a_static_split_scratch_floats() floats = 32 MiB on every GPU that
- * loads the library, held until the process exits).  The source pages have no
- * counterpart: this is an interface convenience, not part of the method.
+ * library: q8a_static_split_scratch_floats() floats = 32 MiB, held until the
+ * process exits on each GPU where the library's kernels are loaded (with the
+ * default lazy module loading, each GPU where one of them first runs; with
+ * CUDA_MODULE_LOADING=EAGER, every visible GPU when the library is loaded).
+ * The source pages have no counterpart: this is an interface convenience, not
+ * part of the method.
  *   Arguments, result and errors: as attn_chunk_step_split without the
  *   workspace.  A call whose partial states would need more floats than the
  *   scratch holds (q8a_split_workspace_floats(...) > the scratch size) is
  *   rejected with Q8A_ERR_INVALID_ARG before anything is launched; use larger
  *   key ranges or attn_chunk_step_split with a workspace of your own.
  *   The first call on a device looks up the scratch's device address on that
- *   (current) device; make that first call before any stream capture.
+ *   (current) device, and looks it up again when the device's context has
+ *   changed since (after cudaDeviceReset); make the first call before any
+ *   stream capture.
  *   Every call on a device shares the one scratch array, which keeps the last
  *   call's contents; each call writes every partial it later reads, so no
  *   clearing is needed, but calls whose kernels can overlap on the GPU (other
- *   streams, other host threads) race on it: order them on one stream.
+ *   streams, other host threads) race on it: order them on one stream.  After
+ *   a timeout the state is undefined, as for attn_chunk_step_split.
  */
 int attn_chunk_step_split_static(const void *q, int64_t q_pos0, const void *k_q8,
                                  const void *v_q8, int64_t kv_plane_stride_bytes,
@@ -232,23 +243,31 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
                   int64_t n_q, int32_t head_dim, void *stream);
 
 /*
- * attn_prefill_pipelined -- the whole prefill from host buffers ([STREAM §2]:
- * the next KV chunk is read while the current one is folded into the state):
- * Q is copied to the device, then for each chunk of `chunk` tokens its K and V
- * are copied on `copy_stream` while `compute_stream` quantises and folds the
- * chunks before it (q8kv_quantize on the chunk's tokens, attn_chunk_step with
- * kv_start = the chunk's first token, q_pos0 = 0).  With `causal` no later
- * chunk touches a chunk's own query rows, so those rows are finalised right
- * after its step and copied back to the host on copy_stream while the device
- * works on the later chunks; without it, attn_finalize and one copy back run
- * at the end.  The result is bit-identical to quantising the whole K and V,
- * folding the same chunks in order and finalising.
+ * attn_prefill_pipelined -- the whole prefill from host buffers ([STREAM §2]
+ * "Double-Buffered Ping-Pong Execution": the next KV chunk is read into the
+ * second of two fixed slots while the current one is folded into the state).
+ * Q is copied to the device, then for each chunk of `chunk` tokens its fp32 K
+ * and V are copied on `copy_stream` into slot c % 2 of `kv_slots` while
+ * `compute_stream` quantises and folds the chunks before it (q8kv_quantize of
+ * the slot into the Q8_0 planes, attn_chunk_step with kv_start = the chunk's
+ * first token, q_pos0 = 0); a slot is refilled only after the quantise that
+ * read it.  The fp32 inputs so take 2 x 2 x B x chunk x H x 64 floats of device
+ * memory whatever the sequence length.  With `causal` no later chunk touches a
+ * chunk's own query rows, so those rows are finalised right after its step and
+ * copied back to the host on copy_stream while the device works on the later
+ * chunks; without it, attn_finalize and one copy back run at the end.  The
+ * result is bit-identical to quantising the whole K and V, folding the same
+ * chunks in order and finalising.
  *   q_host, out_host   fp16 [B][n_tokens][H][64] in host memory;
  *   k_host, v_host     fp32 [B][n_tokens][H][64] in host memory;
  *                      page-locked host memory lets the copies overlap the
  *                      device work (pageable memory works, without overlap).
- *   q_dev, k_dev, v_dev, out_dev  device buffers of the same layouts and sizes;
- *   k8, v8, plane_stride_bytes    the Q8_0 planes (as for q8kv_quantize);
+ *   q_dev, out_dev     device buffers of the layout and size of q_host;
+ *   kv_slots           device fp32 scratch, 16-byte aligned, of at least
+ *                      q8a_prefill_slot_floats(batch, heads, min(chunk,
+ *                      n_tokens)) floats (kv_slot_floats); overwritten;
+ *   k8, v8, plane_stride_bytes    the Q8_0 planes of the whole sequence (as for
+ *                      q8kv_quantize): the cache this prefill produces;
  *   m, l, o            the state (as for attn_state_init; initialised here);
  *   chunk              tokens per chunk, a positive multiple of 4;
  *   compute_stream, copy_stream   two streams (the same stream is allowed and
@@ -257,16 +276,21 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  *                      work already on the compute stream, so back-to-back calls
  *                      on the same buffers are ordered.  The output is on the
  *                      host once compute_stream has drained.
- * The call creates and releases two CUDA events; it allocates no memory.
- * Errors: Q8A_ERR_INVALID_ARG (sizes, null pointers), those of the calls above,
- * Q8A_ERR_CUDA (a copy, event or stream call failed).
+ * The call creates and releases four CUDA events; it allocates no memory.
+ * Errors: Q8A_ERR_INVALID_ARG (sizes, null pointers, too small kv_slots),
+ * Q8A_ERR_MISALIGNED, those of the calls above, Q8A_ERR_CUDA (a copy, event or
+ * stream call failed).
  */
 int attn_prefill_pipelined(const void *q_host, const float *k_host, const float *v_host,
                            void *out_host, int64_t batch, int32_t heads, int64_t n_tokens,
                            int32_t head_dim, int64_t chunk, float scale, int32_t causal,
-                           void *q_dev, float *k_dev, float *v_dev, void *k8, void *v8,
-                           int64_t plane_stride_bytes, float *m, float *l, float *o,
+                           void *q_dev, float *kv_slots, int64_t kv_slot_floats, void *k8,
+                           void *v8, int64_t plane_stride_bytes, float *m, float *l, float *o,
                            void *out_dev, void *compute_stream, void *copy_stream);
+
+/* Floats of kv_slots attn_prefill_pipelined needs: 4 * batch * chunk * heads * 64
+ * (two slots of one chunk's fp32 K and V); -1 for invalid sizes. */
+int64_t q8a_prefill_slot_floats(int64_t batch, int32_t heads, int64_t chunk);
 
 /*
  * q8a_device_status -- read (and optionally clear) the status word of the

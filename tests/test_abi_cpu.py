@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), f"missing export {n}"
         assert n in q8attn.SIGNATURES, f"binding lacks {n}"
-    assert lib.q8a_abi_version() == 2
+    assert lib.q8a_abi_version() == 3
 
 
 def test_plane_stride(lib):
@@ -157,14 +157,23 @@ def test_pipelined_prefill_validation(lib):
     """attn_prefill_pipelined checks sizes and pointers before any CUDA call."""
     from chunked_prefill_attention_gb300 import q8attn as Q
 
-    def call(chunk=256, hd=64, q=A16, B=1, M=512):
-        return lib.attn_prefill_pipelined(q, A16, A16, A16, B, 2, M, hd, chunk, 0.125, 1, A16, A16, A16,
-                                          A16, A16, 34816, A16, A16, A16, A16, P(0), P(0))
+    def call(chunk=256, hd=64, q=A16, B=1, M=512, slots=A16, slot_floats=None):
+        if slot_floats is None:
+            slot_floats = lib.q8a_prefill_slot_floats(B, 2, min(chunk, M) if chunk > 0 else 1)
+        return lib.attn_prefill_pipelined(q, A16, A16, A16, B, 2, M, hd, chunk, 0.125, 1, A16, slots,
+                                          slot_floats, A16, A16, 34816, A16, A16, A16, A16, P(0), P(0))
 
+    assert lib.q8a_prefill_slot_floats(2, 3, 100) == 4 * 2 * 100 * 3 * 64
+    assert lib.q8a_prefill_slot_floats(1, 0, 100) == -1
     assert call(chunk=0) == Q.Q8A_ERR_INVALID_ARG
     assert call(chunk=6) == Q.Q8A_ERR_INVALID_ARG
     assert call(hd=128) == Q.Q8A_ERR_INVALID_ARG
     assert call(q=P(0)) == Q.Q8A_ERR_INVALID_ARG
+    assert call(slots=P(0)) == Q.Q8A_ERR_INVALID_ARG
+    # two slots of one 256-token chunk are needed, whatever the sequence length
+    assert call(slot_floats=lib.q8a_prefill_slot_floats(1, 2, 256) - 1) == Q.Q8A_ERR_INVALID_ARG
+    assert b"kv_slots" in lib.q8a_last_error()
+    assert call(slots=P(0x100008)) == Q.Q8A_ERR_MISALIGNED
     assert call(B=0) == Q.Q8A_OK
     assert call(M=0) == Q.Q8A_OK
 

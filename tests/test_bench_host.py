@@ -72,3 +72,14 @@ def test_quantize_roofline_counts_fp32_in_and_q8_0_out():
     assert abs(rec["achieved"] - rec["algorithmic_bytes"] / 0.2e-3 / 1e9) < 1e-6
     assert abs(rec["frac"] - rec["achieved"] / 6795.1) < 1e-12
     assert rec["bound"] == "hbm" and rec["unit"] == "GB/s"
+
+
+def test_step_bytes_of_the_smallest_workload():
+    """m512 (1 x 512 tokens, 32 heads, chunks of 128): quantise 2 x 324 B, init
+    264 B and finalise 388 B per state row, and per chunk 656 B per state row
+    at or after the chunk start plus 136 B per chunk key and head."""
+    import bench
+    from chunked_prefill_attention_gb300 import workloads as W
+    rows = 32 * 512
+    chunks = sum(32 * (512 - s0) * 656 + 32 * 128 * 136 for s0 in (0, 128, 256, 384))
+    assert bench.step_hbm_bytes(W.WORKLOADS["m512"]) == rows * (2 * 324 + 264 + 388) + chunks

@@ -12,8 +12,11 @@ from tests.parity import assert_device_clean, compare, oracle_out, seeded
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
 
 
-@pytest.mark.parametrize("B,M,H,chunk", [(1, 1000, 2, 256), (2, 768, 3, 128), (1, 2048, 4, 2048)])
+@pytest.mark.parametrize("B,M,H,chunk", [(1, 1000, 2, 256), (2, 768, 3, 128), (1, 2048, 4, 2048),
+                                         (2, 2600, 3, 256)])
 def test_pipelined_matches_device_path(lib, B, M, H, chunk):
+    """The K/V slots hold two chunks: with M > 2 * chunk each slot is refilled
+    several times (the last case streams 11 chunks through them)."""
     from chunked_prefill_attention_gb300 import q8attn as Q
     q = seeded((B, M, H, 64), M + 71, "cuda", torch.float16)
     k = seeded((B, M, H, 64), M + 72, "cuda")
@@ -21,10 +24,11 @@ def test_pipelined_matches_device_path(lib, B, M, H, chunk):
     ref, *_ = Q.prefill_attention(q, k, v, chunk)
     qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
     oh = torch.empty((B, M, H, 64), dtype=torch.float16).pin_memory()
-    bufs = Q.PipelineBuffers(B, M, H, q.device)
+    bufs = Q.PipelineBuffers(B, M, H, q.device, chunk)
+    assert bufs.kv_slots.numel() == 4 * B * min(chunk, M) * H * 64   # two chunks of K and V
     for _ in range(2):   # twice on the same buffers: the calls must be ordered
         oh.zero_()
-        Q.attn_prefill_pipelined(qh, kh, vh, oh, chunk, bufs)
+        Q.attn_prefill_pipelined(qh, kh, vh, oh, bufs)
         torch.cuda.current_stream().synchronize()
         assert_device_clean()
         assert torch.equal(oh, ref.cpu())
@@ -43,8 +47,8 @@ def test_pipelined_without_causal_mask(lib, B, M, H, chunk):
     ref, *_ = Q.prefill_attention(q, k, v, chunk, causal=False)
     qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
     oh = torch.zeros((B, M, H, 64), dtype=torch.float16).pin_memory()
-    bufs = Q.PipelineBuffers(B, M, H, q.device)
-    Q.attn_prefill_pipelined(qh, kh, vh, oh, chunk, bufs, causal=False)
+    bufs = Q.PipelineBuffers(B, M, H, q.device, chunk)
+    Q.attn_prefill_pipelined(qh, kh, vh, oh, bufs, causal=False)
     torch.cuda.current_stream().synchronize()
     assert_device_clean()
     assert torch.equal(oh, ref.cpu())

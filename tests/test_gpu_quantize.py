@@ -114,3 +114,28 @@ def test_quantize_m1m_sampled_windows(lib):
             want = oracle_runner.quantize_kv(x[:, s0:s0 + 256].cpu().numpy())
             assert np.array_equal(got, want), f"window at token {s0}"
         del out
+
+
+def test_quantize_scale_overflow_gives_zero_codes(lib):
+    """A block with amax beyond 65504 * 127 has its scale rounded to +inf in
+    fp16; the oracle's codes are then x / inf = 0 (outside the documented
+    input range, but still bit-exact)."""
+    B, M, H = 1, 32, 4
+    x = seeded((B, M, H, 64), 17, "cuda")
+    x[0, 3, 1, :32] = 1.0e7 * torch.sign(x[0, 3, 1, :32])
+    x[0, 9, 2, 32:] = -9.0e6
+    out = _check(x, lib)
+    raw = gpu_bytes(out, M)
+    assert raw[0, 1, 3, 0:2].tobytes() == np.float16(np.inf).tobytes()
+    assert not raw[0, 1, 3, 2:34].any()
+
+
+@pytest.mark.parametrize("offset_floats", [4, 8])
+def test_quantize_input_only_16_byte_aligned(lib, offset_floats):
+    """An input 16 but not 32 bytes aligned is read with 128-bit loads; the
+    bytes are the same."""
+    B, M, H = 2, 50, 3
+    base = seeded((B * M * H * 64 + offset_floats,), 23, "cuda")
+    x = base[offset_floats:].view(B, M, H, 64)
+    assert x.data_ptr() % 16 == 0
+    _check(x, lib)

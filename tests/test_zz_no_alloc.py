@@ -1,9 +1,12 @@
 """attn_chunk_step_split_static: the split chunk step for callers that cannot
-allocate device memory at call time (its partial states live in a fixed
-scratch array inside the library).  Checked through the C ABI against
-attn_chunk_step_split with a workspace of the caller's own, on two different
-problems in a row (the shared scratch keeps the first call's contents when the
-second one runs).  This file is collected last on purpose."""
+allocate device memory at call time, such as code inside a host framework that
+owns the device allocator, or a loop that cannot take the implicit device
+synchronisation of cudaMalloc (its partial states live in a fixed scratch array
+inside the library).  Checked through the C ABI against attn_chunk_step_split
+with a workspace of the caller's own, on two different problems in a row (the
+shared scratch keeps the first call's contents when the second one runs), and
+against the oracle; and checked to take no device memory once loaded.  This
+file is collected last on purpose."""
 
 import ctypes
 import math
@@ -44,7 +47,12 @@ def test_static_scratch_limit_is_checked(lib):
 @pytest.mark.gpu
 @pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")
 def test_static_split_matches_workspace_split_twice(lib):
+    """Two different problems in a row: the static scratch still holds the
+    first problem's partials when the second runs.  The static call runs the
+    same kernels on the same inputs as the workspace call, so m, l, O and the
+    output must be identical; both are also checked against the oracle."""
     from chunked_prefill_attention_gb300 import q8attn as Q
+    from tests.parity import compare, oracle_out
     cases = [
         # 64 candidates after a 4,096-token context, rectangular mask
         dict(M=4096, H=4, n_q=64, q_pos0=4096, causal=False, split=512, chunk=4096, seed=901),
@@ -66,7 +74,32 @@ def test_static_split_matches_workspace_split_twice(lib):
             rc = _call_static(lib, q, k8, v8, s0, n, got, c["split"], c["q_pos0"], c["causal"],
                               k_off=s0 * 68)
             assert rc == Q.Q8A_OK, lib.q8a_last_error()
-        want, out = Q.attn_finalize(ref).float(), Q.attn_finalize(got).float()
+        want, out = Q.attn_finalize(ref), Q.attn_finalize(got)
         assert_device_clean()
-        assert torch.max(torch.abs(out - want)).item() <= MAX_ABS
-        assert torch.equal(ref.m, got.m)
+        assert torch.equal(ref.m, got.m) and torch.equal(ref.l, got.l) and torch.equal(ref.o, got.o)
+        assert torch.equal(out, want)
+        oracle, _, _ = oracle_out(q, k, v, causal=c["causal"], q_pos0=c["q_pos0"])
+        compare(out.cpu().numpy(), oracle, f"static split M={M} n_q={n_q}")
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")
+def test_static_split_takes_no_device_memory(lib):
+    """After a first call (which loads the kernels and makes the scratch
+    resident), further calls leave the free device memory unchanged."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    M, H, n_q = 2048, 2, 64
+    q = seeded((1, n_q, H, 64), 931, "cuda", torch.float16)
+    k8 = Q.q8kv_quantize(seeded((1, M, H, 64), 932, "cuda"))
+    v8 = Q.q8kv_quantize(seeded((1, M, H, 64), 933, "cuda"))
+    st = Q.State(1, H, n_q, q.device)
+    assert _call_static(lib, q, k8, v8, 0, M, st, 256, M, False) == Q.Q8A_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        Q.attn_state_init(st)
+        assert _call_static(lib, q, k8, v8, 0, M, st, 256, M, False) == Q.Q8A_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert_device_clean()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
