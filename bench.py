@@ -103,6 +103,15 @@ def quantize_record(B, M, H, D, ms, peaks, peak_src):
             "frac": gbs / hbm if gbs else None, "peak_kind": f"HBM copy, {peak_src}"}
 
 
+def hbm_record(kernel, n_bytes, ms, peaks, peak_src, algorithmic):
+    """HBM roofline of one launch per step of an HBM-bound kernel."""
+    gbs = n_bytes / (ms * 1e-3) / 1e9 if ms > 0 else None
+    hbm = float(peaks.get("hbm_gbs"))
+    return {"kernel": kernel, "bound": "hbm", "ms_per_step": ms, "algorithmic_bytes": n_bytes,
+            "algorithmic": algorithmic, "achieved": gbs, "peak": hbm, "unit": "GB/s",
+            "frac": gbs / hbm if gbs else None, "peak_kind": f"HBM copy, {peak_src}"}
+
+
 def make_record(*, value, n_gpus, steps, warmup, ms_per_step, config, extra):
     rec = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": steps,
@@ -312,13 +321,19 @@ def run_ours(args):
         if qev is not None:
             qev[1].record(stream)
         Q.attn_state_init(st)
+        if qev is not None:
+            qev[2].record(stream)
         for i, (s0, n) in enumerate(chunks):
             if ev is not None:
                 ev[i][0].record(stream)
             Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * 68)
             if ev is not None:
                 ev[i][1].record(stream)
+        if qev is not None:
+            qev[3].record(stream)
         Q.attn_finalize(st, out)
+        if qev is not None:
+            qev[4].record(stream)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -329,8 +344,7 @@ def run_ours(args):
 
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in chunks]
            for _ in range(args.steps)]
-    qevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
+    qevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = None if args.no_clocks else ClockSampler(local_rank)
     dist_barrier(dist)
@@ -346,7 +360,9 @@ def run_ours(args):
     clk = clocks.stop() if clocks else None
     ms = t0.elapsed_time(t1) / args.steps
     chunk_ms = sum(a.elapsed_time(b) for per in evs for a, b in per) / args.steps
-    quant_ms = sum(a.elapsed_time(b) for a, b in qevs) / args.steps
+    quant_ms = sum(e[0].elapsed_time(e[1]) for e in qevs) / args.steps
+    init_ms = sum(e[1].elapsed_time(e[2]) for e in qevs) / args.steps
+    fin_ms = sum(e[3].elapsed_time(e[4]) for e in qevs) / args.steps
     launches_chunk = len(chunks)
     ms_max = dist_max(dist, ms)
     rc, status = Q.device_status()
@@ -428,6 +444,10 @@ def run_ours(args):
                      "algorithmic": "4*D flops per unmasked (query, key) pair; %d launches/step" % launches_chunk,
                      "traffic": traffic, "traffic_note": traffic_state},
         "quantize": quantize_record(B, M, H, D, quant_ms, peaks, peak_src),
+        "state_init": hbm_record("attn_state_init", B * H * M * 264, init_ms, peaks, peak_src,
+                                 "264 B written per state row (m, l, 64 O)"),
+        "finalize": hbm_record("attn_finalize", B * H * M * 388, fin_ms, peaks, peak_src,
+                               "260 B read (l, 64 O) + 128 B fp16 written per state row"),
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": n_launch,

@@ -914,6 +914,18 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
     e = cudaFuncSetAttribute(chunk_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // The setmaxnreg split assumes every thread is launched with 65536 / 512
+    // registers; with fewer, an increase could wait forever, so such a build is
+    // refused before any launch.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, chunk_step_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads != 65536 || fa.maxThreadsPerBlock < kThreads) {
+      set_launch_note("chunk_step_kernel has %d registers per thread and at most %d threads per "
+                      "block; the register split needs %d and %d",
+                      fa.numRegs, fa.maxThreadsPerBlock, 65536 / kThreads, kThreads);
+      return cudaErrorInvalidConfiguration;
+    }
     configured_device = dev;
   }
   // the host counts 128-row query tiles; a CTA takes NQT of them
@@ -924,7 +936,11 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const unsigned gy = args.split_keys > 0 ? static_cast<unsigned>(args.n_splits) : 1u;
   chunk_step_kernel<<<dim3(static_cast<unsigned>(blocks), gy), kThreads, SMEM_BYTES, stream>>>(qmap, units);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess)
+    set_launch_note("chunk_step_kernel<<<(%lld, %u), %d, %d>>>", static_cast<long long>(blocks), gy,
+                    kThreads, SMEM_BYTES);
+  return e;
 }
 
 cudaError_t read_device_status(cudaStream_t stream, uint32_t* status, bool clear) {

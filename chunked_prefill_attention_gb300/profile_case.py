@@ -12,6 +12,13 @@ diagonal), and the device holds about 0.3 GB, above the 129 MB L2.
   ncu --set full --clock-control none -k regex:chunk_step_kernel -s 2 -c 1 \\
       python -m chunked_prefill_attention_gb300.profile_case
 
+With --quantize TOKENS it runs q8kv_quantize instead: the K of the m64k draw
+at TOKENS tokens (65536: 537 MB of fp32 in, 143 MB of Q8_0 out, above L2), one
+warm-up launch and then --reps launches.
+
+  ncu --set full --clock-control none -k regex:q8kv_quantize -s 1 -c 1 \\
+      python -m chunked_prefill_attention_gb300.profile_case --quantize 65536
+
 With --burst CONTEXT it runs Mode B burst verification instead: the 64
 candidates of the burst_m1m draw against a CONTEXT-token, 32-head Q8_0 cache
 in key ranges of --split keys (attn_chunk_step_split, paired launches), one
@@ -36,10 +43,13 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=2)
     p.add_argument("--burst", type=int, default=0)
     p.add_argument("--split", type=int, default=8192)
+    p.add_argument("--quantize", type=int, default=0)
     a = p.parse_args(argv)
     _build.ensure_built()
     if a.burst > 0:
         return burst(a)
+    if a.quantize > 0:
+        return quantize(a)
     w = W.WORKLOADS["m64k"]
     q, k, v = W.make_inputs(w, device="cuda", tokens=a.tokens)
     B, M, H, _ = q.shape
@@ -62,6 +72,26 @@ def main(argv=None):
     rows = M - (s0 // 128) * 128
     print(f"chunk {a.index} (keys {s0}..{s0 + n - 1}, query rows {s0 // 128 * 128}..{M - 1}): "
           f"{ms:.3f} ms per launch, status {rc}")
+
+
+def quantize(a):
+    import torch
+
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
+
+    w = W.WORKLOADS["m64k"]
+    _, k, _ = W.make_inputs(w, device="cuda", tokens=a.quantize)
+    k8 = Q.q8kv_quantize(k)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(a.reps):
+        Q.q8kv_quantize(k, k8)
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / a.reps
+    B, M, H, D = k.shape
+    n_bytes = B * M * H * (D * 4 + 68)
+    print(f"quantize {B}x{M}x{H}x{D}: {ms:.4f} ms per launch, {n_bytes / (ms * 1e-3) / 1e9:.0f} GB/s")
 
 
 def burst(a):

@@ -297,7 +297,8 @@ int64_t q8a_prefill_slot_floats(int64_t batch, int32_t heads, int64_t chunk);
  * current device: 0 when no device-side wait has run out since the last clear.
  * Synchronises `stream`.  Returns Q8A_OK, Q8A_ERR_TIMEOUT (when the word is
  * nonzero; *status_out then holds it: bit 0 set, bits 8..15 the role that gave
- * up first) or Q8A_ERR_CUDA.  status_out may be NULL.
+ * up first: 1 softmax, 2 dequantisation, 3 producer, 4 MMA issue, 5 final drain)
+ * or Q8A_ERR_CUDA.  status_out may be NULL.
  */
 int q8a_device_status(void *stream, uint32_t *status_out, int32_t clear);
 
