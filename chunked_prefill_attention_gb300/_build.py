@@ -65,6 +65,43 @@ def build(verbose=False):
     return LIB
 
 
+SANITIZED_LIB = os.path.join(PKG, "libq8attn_sanitized.so")
+HOST_SOURCES = ["api.cu", "pipeline.cu"]   # the C-ABI layer: validation, streams, events
+
+
+def build_sanitized():
+    """libq8attn_sanitized.so: the same library with the host code of the C-ABI
+    layer built with AddressSanitizer and UndefinedBehaviorSanitizer (the
+    kernels are unchanged).  Load it with the sanitizer runtime preloaded."""
+    os.makedirs(BUILD, exist_ok=True)
+    nvcc = _nvcc()
+    # one flag per -Xcompiler: nvcc splits its arguments at commas
+    san = [f"-Xcompiler={f}" for f in ("-fsanitize=address", "-fsanitize=undefined",
+                                        "-fno-omit-frame-pointer", "-fno-sanitize-recover=all")]
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + (".san.o" if src in HOST_SOURCES else ".o"))
+        if src not in HOST_SOURCES and os.path.exists(obj) and os.path.getmtime(obj) > os.path.getmtime(
+                os.path.join(CSRC, src)):
+            return obj
+        cmd = [nvcc, *_flags(), *(san if src in HOST_SOURCES else []), "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = SANITIZED_LIB + ".tmp"
+    cmd = [nvcc, ARCH, "-shared", "-Xcompiler=-fsanitize=address", "-Xcompiler=-fsanitize=undefined", "-o",
+           tmp] + objs
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, SANITIZED_LIB)
+    return SANITIZED_LIB
+
+
 def ensure_built():
     if _stale():
         build()

@@ -14,7 +14,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libq8attn.so")
+# Q8ATTN_LIBRARY selects another in-tree build of the same library (the
+# sanitizer build the host-code tests load); it is never a fallback.
+LIB_PATH = os.environ.get("Q8ATTN_LIBRARY") or os.path.join(_HERE, "libq8attn.so")
 
 Q8A_OK = 0
 Q8A_ERR_INVALID_ARG = -1

@@ -22,8 +22,10 @@ def cuda_available():
 
 @pytest.fixture(scope="session")
 def lib():
-    """The C-ABI library, built in-tree if it is missing."""
-    from chunked_prefill_attention_gb300 import _build
-    _build.ensure_built()
+    """The C-ABI library, built in-tree if it is missing (or the prebuilt one
+    that Q8ATTN_LIBRARY names, which is loaded as it is)."""
+    if not os.environ.get("Q8ATTN_LIBRARY"):
+        from chunked_prefill_attention_gb300 import _build
+        _build.ensure_built()
     from chunked_prefill_attention_gb300 import q8attn
     return q8attn.load()
