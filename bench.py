@@ -48,7 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
-    p.add_argument("--other-workloads", default="m512,m2k_out,b8_m2k,m1m",
+    p.add_argument("--other-workloads", default="m512,m2k_out,b8_m2k,m1m,m16k_d128",
                    help="comma-separated workloads also timed (one GPU only) and reported under "
                         "'workloads'; empty to skip")
     return p.parse_args(argv)
@@ -198,17 +198,21 @@ def profile_traffic(kernel_src):
 
 
 def step_hbm_bytes(w):
-    """Algorithmic HBM bytes of one step of workload w: quantise K and V (256 B
-    fp32 in + 68 B Q8_0 out per head row each), state init (264 B per state
-    row), one chunk step per KV chunk (per state row it touches: 128 B of Q and
-    2 x 264 B of state; per chunk key and head: 136 B of Q8_0 K and V), finalise
-    (260 B in + 128 B out per state row)."""
-    B, M, H = w.batch, w.tokens, w.heads
+    """Algorithmic HBM bytes of one step of workload w (head_dim D; the figures
+    in brackets are D = 64): quantise K and V (4D B fp32 in + D/32*34 B Q8_0 out
+    per head row each [256 + 68]), state init (4(2 + D) B per state row [264]),
+    one chunk step per KV chunk (per state row it touches: 2D B of Q and
+    2 x 4(2 + D) B of state [128 + 528]; per chunk key and head: 2 x D/32*34 B
+    of Q8_0 K and V [136]), finalise (4(1 + D) B in + 2D B out per state row
+    [260 + 128])."""
+    B, M, H, D = w.batch, w.tokens, w.heads, w.head_dim
+    row8 = D // 32 * 34
+    state = 4 * (2 + D)
     rows = B * H * M
-    total = 2 * rows * 324 + rows * 264 + rows * 388
+    total = 2 * rows * (4 * D + row8) + rows * state + rows * (4 * (1 + D) + 2 * D)
     for s0 in range(0, M, w.chunk):
         n = min(w.chunk, M - s0)
-        total += B * H * (M - s0) * (128 + 528) + B * H * n * 136
+        total += B * H * (M - s0) * (2 * D + 2 * state) + B * H * n * 2 * row8
     return total
 
 
@@ -223,10 +227,10 @@ def time_workload(name, steps, warmup, peaks, peak_src, flush_l2, sample_clocks)
     dev = torch.cuda.current_device()
     B, M, H, D = w.batch, w.tokens, w.heads, w.head_dim
     q, k, v = W.make_inputs(w, device=torch.device("cuda", dev))
-    stride = Q.plane_stride(M)
+    stride = Q.plane_stride(M, D)
     k8 = torch.empty((B, H, stride), dtype=torch.uint8, device=q.device)
     v8 = torch.empty((B, H, stride), dtype=torch.uint8, device=q.device)
-    st = Q.State(B, H, M, q.device, init=False)
+    st = Q.State(B, H, M, q.device, init=False, head_dim=D)
     out = torch.empty((B, M, H, D), dtype=torch.float16, device=q.device)
     chunks = [(s0, min(w.chunk, M - s0)) for s0 in range(0, M, w.chunk)]
     stream = torch.cuda.current_stream()
@@ -241,7 +245,7 @@ def time_workload(name, steps, warmup, peaks, peak_src, flush_l2, sample_clocks)
         if ev is not None:
             ev[1].record(stream)
         for s0, n in chunks:
-            Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * 68)
+            Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * Q.row_bytes(D))
         if ev is not None:
             ev[2].record(stream)
         Q.attn_finalize(st, out)
@@ -271,7 +275,7 @@ def time_workload(name, steps, warmup, peaks, peak_src, flush_l2, sample_clocks)
            "tokens_per_s": B * M / (ms * 1e-3), "steps": steps, "warmup": warmup,
            "l2": ("L2 flushed before each step (256 MB write outside the timed events)" if flush_l2
                   else "inputs larger than L2")}
-    if w.tokens >= 65536:
+    if w.tokens >= 65536 or D == 128:
         peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
         achieved = w.causal_flops / (chunk_ms * 1e-3) / 1e12
         rec["roofline"] = {"bound": "tensor", "kernel": "attn_chunk_step", "achieved": achieved,

@@ -77,12 +77,18 @@ void q8a::set_launch_note(const char* fmt, ...) {
 
 namespace {
 
-int check_common(int64_t batch, int32_t heads, int32_t head_dim, const char* fn) {
+// allow_128: the call also supports head_dim 128 (four Q8_0 blocks per row).
+int check_common(int64_t batch, int32_t heads, int32_t head_dim, const char* fn, bool allow_128) {
   if (batch < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: batch must be >= 0 (got %lld)", fn, (long long)batch);
   if (heads <= 0) return fail(Q8A_ERR_INVALID_ARG, "%s: heads must be > 0 (got %d)", fn, heads);
-  if (head_dim != 64) return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 (got %d)", fn, head_dim);
+  if (head_dim != 64 && !(allow_128 && head_dim == 128))
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64%s (got %d)", fn, allow_128 ? " or 128" : "",
+                head_dim);
   return Q8A_OK;
 }
+
+// Bytes of one Q8_0 head row: head_dim / 32 blocks of 34 bytes.
+int64_t row_bytes(int32_t head_dim) { return static_cast<int64_t>(head_dim / 32) * 34; }
 
 }  // namespace
 
@@ -97,21 +103,28 @@ int64_t q8a_plane_stride_bytes(int64_t n_tokens) {
   return (n_tokens * Q8A_ROW_BYTES + 15) / 16 * 16;
 }
 
+int64_t q8a_plane_stride_bytes_for(int64_t n_tokens, int32_t head_dim) {
+  if (n_tokens < 0 || (head_dim != 64 && head_dim != 128)) return -1;
+  return (n_tokens * row_bytes(head_dim) + 15) / 16 * 16;
+}
+
 int q8kv_quantize(const float* x, void* q8_out, int64_t batch, int64_t n_tokens, int32_t heads,
                   int32_t head_dim, int64_t out_plane_stride_bytes, void* stream) {
   q8a::NvtxRange nvtx_range("q8kv_quantize");
   const char* fn = "q8kv_quantize";
-  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (int rc = check_common(batch, heads, head_dim, fn, true)) return rc;
   if (n_tokens < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_tokens must be >= 0", fn);
   if (batch == 0 || n_tokens == 0) return ok();
   if (!x || !q8_out) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
-  if (out_plane_stride_bytes < n_tokens * Q8A_ROW_BYTES)
-    return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < n_tokens*68 = %lld", fn,
-                (long long)out_plane_stride_bytes, (long long)(n_tokens * Q8A_ROW_BYTES));
+  if (out_plane_stride_bytes < n_tokens * row_bytes(head_dim))
+    return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < n_tokens*%lld = %lld", fn,
+                (long long)out_plane_stride_bytes, (long long)row_bytes(head_dim),
+                (long long)(n_tokens * row_bytes(head_dim)));
   if (!aligned(x, 16) || !aligned(q8_out, 16) || out_plane_stride_bytes % 16)
     return fail(Q8A_ERR_MISALIGNED, "%s: x, q8_out and the plane stride must be 16-byte aligned", fn);
   cudaError_t e = q8a::launch_quantize(x, static_cast<uint8_t*>(q8_out), batch, n_tokens, heads,
-                                       out_plane_stride_bytes, static_cast<cudaStream_t>(stream));
+                                       head_dim, out_plane_stride_bytes,
+                                       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }
@@ -120,13 +133,14 @@ int attn_state_init(float* m, float* l, float* o, int64_t batch, int32_t heads, 
                     int32_t head_dim, void* stream) {
   q8a::NvtxRange nvtx_range("attn_state_init");
   const char* fn = "attn_state_init";
-  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (int rc = check_common(batch, heads, head_dim, fn, true)) return rc;
   if (n_q < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q must be >= 0", fn);
   if (batch == 0 || n_q == 0) return ok();
   if (!m || !l || !o) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (!aligned(m, 4) || !aligned(l, 4) || !aligned(o, 16))
     return fail(Q8A_ERR_MISALIGNED, "%s: m, l need 4-byte and o 16-byte alignment", fn);
-  cudaError_t e = q8a::launch_state_init(m, l, o, batch * heads * n_q, static_cast<cudaStream_t>(stream));
+  cudaError_t e = q8a::launch_state_init(m, l, o, batch * heads * n_q, head_dim,
+                                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }
@@ -141,7 +155,7 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
                        int64_t n_q, int32_t head_dim, float scale, int32_t causal,
                        CUtensorMap* qmap, q8a::ChunkArgs* a, bool* empty) {
   *empty = false;
-  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (int rc = check_common(batch, heads, head_dim, fn, true)) return rc;
   if (n_q < 0 || kv_len < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q and kv_len must be >= 0", fn);
   if (q_pos0 < 0 || kv_start < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: positions must be >= 0", fn);
   if (!(scale > 0.0f) || !std::isfinite(scale))
@@ -151,14 +165,15 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
     return Q8A_OK;
   }
   if (!q || !k_q8 || !v_q8 || !m || !l || !o) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
-  if (kv_plane_stride_bytes < kv_len * Q8A_ROW_BYTES)
-    return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < kv_len*68 = %lld", fn,
-                (long long)kv_plane_stride_bytes, (long long)(kv_len * Q8A_ROW_BYTES));
+  if (kv_plane_stride_bytes < kv_len * row_bytes(head_dim))
+    return fail(Q8A_ERR_INVALID_ARG, "%s: plane stride %lld < kv_len*%lld = %lld", fn,
+                (long long)kv_plane_stride_bytes, (long long)row_bytes(head_dim),
+                (long long)(kv_len * row_bytes(head_dim)));
   if (!aligned(q, 16) || !aligned(k_q8, 16) || !aligned(v_q8, 16) || kv_plane_stride_bytes % 16 ||
       !aligned(o, 16) || !aligned(m, 4) || !aligned(l, 4))
     return fail(Q8A_ERR_MISALIGNED,
                 "%s: q, k_q8, v_q8, o and the plane stride need 16-byte alignment; m, l 4-byte", fn);
-  if (kv_len > 0x7FFFFFFFll || n_q > 0x7FFFFFFFll || (int64_t)heads * 64 * 2 * n_q >= (1ll << 40))
+  if (kv_len > 0x7FFFFFFFll || n_q > 0x7FFFFFFFll || (int64_t)heads * head_dim * 2 * n_q >= (1ll << 40))
     return fail(Q8A_ERR_UNSUPPORTED, "%s: sizes beyond the supported range", fn);
 
   // Query tiles that can see any key of this chunk.
@@ -179,10 +194,13 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
   std::memset(qmap, 0, sizeof(*qmap));
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(heads) * 64, static_cast<cuuint64_t>(n_q),
+  // the box is 64 channels (128 bytes, one swizzle atom) wide at either head_dim;
+  // a head_dim 128 query tile takes two loads
+  const cuuint64_t hd = static_cast<cuuint64_t>(head_dim);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(heads) * hd, static_cast<cuuint64_t>(n_q),
                               static_cast<cuuint64_t>(batch)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * 64 * 2,
-                                 static_cast<cuuint64_t>(heads) * 64 * 2 * static_cast<cuuint64_t>(n_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * hd * 2,
+                                 static_cast<cuuint64_t>(heads) * hd * 2 * static_cast<cuuint64_t>(n_q)};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult cr = enc(qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q), dims, strides,
@@ -210,6 +228,7 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
   a->scale_log2 = scale * 1.4426950408889634f;
   a->causal = causal ? 1 : 0;
   a->pair = (!causal && n_qtiles == 1) ? 1 : 0;
+  a->head_dim = head_dim;
   a->timeout_ns = g_timeout_ns.load();
   return Q8A_OK;
 }
@@ -231,7 +250,8 @@ int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void*
     return rc;
   if (empty) return ok();
   a.inject = g_inject.exchange(0);
-  cudaError_t e = q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, static_cast<cudaStream_t>(stream))
+                                  : q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }
@@ -262,7 +282,8 @@ int attn_chunk_step_gqa(const void* q, int64_t q_pos0, const void* k_q8, const v
   if (empty) return ok();
   a.kv_heads = kv_heads;
   a.inject = g_inject.exchange(0);
-  cudaError_t e = q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, static_cast<cudaStream_t>(stream))
+                                  : q8a::launch_chunk_step(qmap, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }
@@ -274,6 +295,8 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
                           float* workspace, int64_t workspace_floats, void* stream) {
   q8a::NvtxRange nvtx_range("attn_chunk_step_split");
   const char* fn = "attn_chunk_step_split";
+  if (head_dim != Q8A_HEAD_DIM)
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 (got %d)", fn, head_dim);
   if (split_keys <= 0 || split_keys % 128 != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
                 fn, (long long)split_keys);
@@ -386,6 +409,8 @@ int attn_chunk_step_split_static(const void* q, int64_t q_pos0, const void* k_q8
                                  int64_t split_keys, void* stream) {
   q8a::NvtxRange nvtx_range("attn_chunk_step_split_static");
   const char* fn = "attn_chunk_step_split_static";
+  if (head_dim != Q8A_HEAD_DIM)
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 (got %d)", fn, head_dim);
   if (split_keys <= 0 || split_keys % 128 != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
                 fn, (long long)split_keys);
@@ -408,13 +433,14 @@ int attn_finalize(const float* l, const float* o, void* out, int64_t batch, int3
                   int64_t n_q, int32_t head_dim, void* stream) {
   q8a::NvtxRange nvtx_range("attn_finalize");
   const char* fn = "attn_finalize";
-  if (int rc = check_common(batch, heads, head_dim, fn)) return rc;
+  if (int rc = check_common(batch, heads, head_dim, fn, true)) return rc;
   if (n_q < 0) return fail(Q8A_ERR_INVALID_ARG, "%s: n_q must be >= 0", fn);
   if (batch == 0 || n_q == 0) return ok();
   if (!l || !o || !out) return fail(Q8A_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (!aligned(l, 4) || !aligned(o, 16) || !aligned(out, 16))
     return fail(Q8A_ERR_MISALIGNED, "%s: l needs 4-byte, o and out 16-byte alignment", fn);
-  cudaError_t e = q8a::launch_finalize(l, o, out, batch, heads, n_q, static_cast<cudaStream_t>(stream));
+  cudaError_t e = q8a::launch_finalize(l, o, out, batch, heads, n_q, head_dim,
+                                       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }

@@ -903,6 +903,549 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// head_dim 128.  A 136-byte Q8_0 row (four blocks) and an O row of 128 fp32
+// channels do not fit the two-query-tile layout above (two 32 KB Q tiles and a
+// 128 KB dequantised 128-key stage leave no room for the raw ring, and two O
+// accumulators with residual halves would need 512 TMEM columns alone).  So a
+// CTA takes one 128-row query tile and both softmax pipelines work on its rows
+// (the paired arrangement above, here with or without the causal mask):
+// pipeline A folds the even 64-key tiles, pipeline B the odd ones, each into
+// its own running state, and A merges B's state at the end with the chunk
+// recurrence.  The two pipelines interleave on the tensor pipe as the two query
+// tiles do above.
+//   QK_x: M = 128, N = 64 keys, 16 MMAs of K = 16 over Q.K_hi and Q.K_lo.
+//   PV_x: M = 128, N = 128 channels, 8 MMAs (P.V_hi and P.V_lo, 4 k-steps each)
+//         accumulating into the same 128 columns of O_x.
+// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384).
+// Shared memory: Q 32 KB (two 64-channel swizzle-atom columns), two
+// dequantised stages of 64 KB (stage x holds pipeline x's key tile: K_hi, K_lo,
+// V_hi, V_lo, each two 8 KB atom columns of 64 keys x 128 B), a two-stage raw
+// ring of 2 x 8,704 B.  Dequantisation: thread k < 64 converts K row k, thread
+// 64 + k V row k, so K and V of a tile are converted at once.
+namespace d128 {
+
+constexpr int D = 128;
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int ROWB = 136;              // four 34-byte Q8_0 blocks
+constexpr int RAWB = BN * ROWB;        // 8704
+constexpr int NR = 2;
+constexpr int kThreads = 512;
+constexpr int kRegSoftmax = 136;   // a 64-score S row; the other warpgroups keep 120
+constexpr int kRegOther = 120;
+static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split");
+
+constexpr int TILE = 16384;                       // one 64-key x 128-channel fp16 tile
+constexpr int DQ_KHI = 0, DQ_KLO = TILE, DQ_VHI = 2 * TILE, DQ_VLO = 3 * TILE;
+constexpr int DEQ_BYTES = 4 * TILE;
+constexpr int ATOMC = 8192;                       // one 64-channel atom column of a tile
+constexpr int OFF_Q = 0;                          // 2 atom columns x (128 rows x 128 B)
+constexpr int OFF_DEQ = 32768;
+constexpr int OFF_RAW = OFF_DEQ + 2 * DEQ_BYTES;  // [NR][K raw | V raw]
+constexpr int OFF_BAR = OFF_RAW + NR * 2 * RAWB;
+constexpr int B_QFULL = 0;
+constexpr int B_RAWFULL = 1;                 // NR
+constexpr int B_RAWEMPTY = B_RAWFULL + NR;   // NR
+constexpr int B_KFULL = B_RAWEMPTY + NR;     // 2 (stage = pipeline)
+constexpr int B_KEMPTY = B_KFULL + 2;
+constexpr int B_VFULL = B_KEMPTY + 2;
+constexpr int B_VEMPTY = B_VFULL + 2;
+constexpr int B_SFULL = B_VEMPTY + 2;
+constexpr int B_PFULL = B_SFULL + 2;
+constexpr int B_ODONE = B_PFULL + 2;
+constexpr int B_MERGE = B_ODONE + 2;
+constexpr int B_DRAIN = B_MERGE + 1;
+constexpr int NBAR = B_DRAIN + 1;
+constexpr int OFF_CTL = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
+constexpr int OFF_XCH = OFF_CTL + CTL_BYTES;      // 128 x float4 {m, l, ok, -} of pipeline B
+constexpr int SMEM_USED = OFF_XCH + BM * 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(OFF_RAW % 16 == 0 && RAWB % 16 == 0, "bulk copy alignment");
+static_assert(OFF_DEQ % 1024 == 0 && TILE % 1024 == 0 && ATOMC % 1024 == 0, "swizzle atom alignment");
+
+constexpr uint32_t T_S = 0;      // + 64 * pipeline
+constexpr uint32_t T_O = 128;    // + 128 * pipeline
+
+struct Unit {
+  int64_t bh, b, h, r0;
+  int T[2];      // key tiles of each pipeline
+  int T_all;
+};
+
+__device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
+  Unit u;
+  const int64_t idx = blockIdx.x;
+  u.bh = idx / a.n_qtiles;
+  const int64_t qt = a.n_qtiles - 1 - (idx % a.n_qtiles);   // heavy tiles first
+  u.b = u.bh / a.heads;
+  u.h = u.bh % a.heads;
+  u.r0 = (static_cast<int64_t>(a.tile0) + qt) * BM;
+  int64_t n_vis = a.kv_len;
+  if (a.causal) {
+    const int64_t r_last = i64min(u.r0 + BM - 1, a.n_q - 1);
+    n_vis = i64min(n_vis, a.q_pos0 + r_last - a.kv_start + 1);
+  }
+  const int tiles = n_vis > 0 ? static_cast<int>((n_vis + BN - 1) / BN) : 0;
+  u.T[0] = (tiles + 1) / 2;
+  u.T[1] = tiles / 2;
+  u.T_all = tiles;
+  return u;
+}
+
+__device__ __forceinline__ void producer(const CUtensorMap* qmap, const ChunkArgs& a, const Unit& u,
+                                         uint8_t* smem, uint32_t sbase, Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  const bool skip_q = (a.inject == 1) && (blockIdx.x == 0);
+  if (lane == 0) {
+    prefetch_tensormap(qmap);
+    if (!skip_q) {
+      mbar_arrive_expect_tx(bar(B_QFULL), BM * D * 2);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(sbase + OFF_Q + c * 16384, qmap, bar(B_QFULL),
+                    static_cast<int32_t>(u.h * D + 64 * c), static_cast<int32_t>(u.r0),
+                    static_cast<int32_t>(u.b));
+    }
+  }
+  int last_bulk[NR];
+#pragma unroll
+  for (int s = 0; s < NR; ++s) last_bulk[s] = -1;
+  const int64_t kv_plane = u.b * a.kv_heads + u.h / (a.heads / a.kv_heads);
+  const uint8_t* kp = a.k8 + kv_plane * a.plane_stride;
+  const uint8_t* vp = a.v8 + kv_plane * a.plane_stride;
+  for (int t = 0; t < u.T_all; ++t) {
+    const int sr = t % NR;
+    if (!wait_bar(bar(B_RAWEMPTY + sr), ((t / NR) & 1) ^ 1, ctl, budget, R_PRODUCER, true)) break;
+    const int64_t k0 = static_cast<int64_t>(t) * BN;
+    const int n = static_cast<int>(i64min(BN, a.kv_len - k0));
+    const uint32_t bytes = static_cast<uint32_t>(n) * ROWB;
+    const uint32_t dk = sbase + OFF_RAW + sr * 2 * RAWB;
+    if ((bytes & 15u) == 0u) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_RAWFULL + sr), 2u * bytes);
+        bulk_load(dk, kp + k0 * ROWB, bytes, bar(B_RAWFULL + sr));
+        bulk_load(dk + RAWB, vp + k0 * ROWB, bytes, bar(B_RAWFULL + sr));
+      }
+#pragma unroll
+      for (int s = 0; s < NR; ++s)
+        if (s == sr) last_bulk[s] = t;
+    } else {
+      // ragged tail whose byte count is not a multiple of 16: plain 4-byte copies
+      const uint32_t* sk = reinterpret_cast<const uint32_t*>(kp + k0 * ROWB);
+      const uint32_t* sv = reinterpret_cast<const uint32_t*>(vp + k0 * ROWB);
+      uint32_t* wk = reinterpret_cast<uint32_t*>(smem + OFF_RAW + sr * 2 * RAWB);
+      uint32_t* wv = wk + RAWB / 4;
+      const int words = n * (ROWB / 4);
+      for (int w = lane; w < words; w += 32) {
+        wk[w] = __ldg(sk + w);
+        wv[w] = __ldg(sv + w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_RAWFULL + sr));
+#pragma unroll
+      for (int s = 0; s < NR; ++s)
+        if (s == sr) last_bulk[s] = -1;
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < NR; ++s)
+    if (last_bulk[s] >= 0) wait_bar(bar(B_RAWFULL + s), (last_bulk[s] / NR) & 1, ctl, budget, R_DRAIN, false);
+  if (!skip_q) wait_bar(bar(B_QFULL), 0, ctl, budget, R_DRAIN, false);
+}
+
+// Thread k < 64: K row k of each tile; thread 64 + k: V row k.  Block b of a
+// 136-byte row (channels 32b .. 32b+31) lands in atom column b / 2, 16-byte
+// chunks 4 (b % 2) .. 4 (b % 2) + 3 of the key's 128-byte row, swizzled.
+__device__ __forceinline__ void dequant(const ChunkArgs& a, const Unit& u, uint8_t* smem,
+                                        uint32_t sbase, Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  const int tid = threadIdx.x - 256;
+  const int tensor = tid >> 6;        // 0: K, 1: V
+  const int k = tid & 63;             // key row of the tile
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  const int sw = k & 7;
+  for (int t = 0; t < u.T_all; ++t) {
+    const int sr = t % NR;
+    const int sd = t & 1;                              // the pipeline reading key tile t
+    const uint32_t fill = static_cast<uint32_t>((t >> 1) & 1);
+    if (!wait_bar(bar(B_RAWFULL + sr), (t / NR) & 1, ctl, budget, R_DEQUANT, true)) break;
+    if (!wait_bar(bar((tensor ? B_VEMPTY : B_KEMPTY) + sd), fill ^ 1, ctl, budget, R_DEQUANT, true)) break;
+    const int n_valid = static_cast<int>(i64min(BN, a.kv_len - static_cast<int64_t>(t) * BN));
+    uint8_t* hi = smem + OFF_DEQ + sd * DEQ_BYTES + (tensor ? DQ_VHI : DQ_KHI) + k * 128;
+    uint8_t* lo = smem + OFF_DEQ + sd * DEQ_BYTES + (tensor ? DQ_VLO : DQ_KLO) + k * 128;
+    if (k < n_valid) {
+      const uint32_t* raw = reinterpret_cast<const uint32_t*>(
+          smem + OFF_RAW + sr * 2 * RAWB + tensor * RAWB + k * ROWB);
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        // 9-word window: even blocks start word-aligned (scale in the low half of
+        // word 0), odd blocks 2 bytes into a word (scale in its high half)
+        const int w0 = 17 * (blk >> 1) + 8 * (blk & 1);
+        uint32_t w[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = raw[w0 + i];
+        dequant_block(w, blk & 1, hi + (blk >> 1) * ATOMC, lo + (blk >> 1) * ATOMC, sw);
+      }
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          *reinterpret_cast<uint4*>(hi + c * ATOMC + 16 * j) = z;
+          *reinterpret_cast<uint4*>(lo + c * ATOMC + 16 * j) = z;
+        }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar((tensor ? B_VFULL : B_KFULL) + sd));
+    mbar_arrive(bar(B_RAWEMPTY + sr));
+  }
+}
+
+__device__ __forceinline__ void mma(const ChunkArgs& a, const Unit& u, uint32_t sbase, uint32_t tmem,
+                                    Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  constexpr uint32_t kIdescQK = idesc_f16_f32(128, BN, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, 0, 1);
+  const bool leader = elect_one();
+  // Q and K tiles K-major in two 64-channel atom columns (16 KB apart for Q,
+  // 8 KB for K); k-step kk covers channels 16kk .. 16kk+15.  V tiles MN-major:
+  // the two 64-channel halves of N are 8 KB apart (leading byte offset), each
+  // k-step covers 16 keys = two 8-row swizzle atoms (2 KB).  P of keys
+  // 16kk .. 16kk+15 sits in TMEM columns 8kk .. 8kk+7 of S_x.
+  const uint64_t qdesc0 = smem_desc(sbase + OFF_Q, 1024, 1024, kSwizzle128);
+  const uint64_t kdesc0 = smem_desc(sbase + OFF_DEQ + DQ_KHI, 1024, 1024, kSwizzle128);
+  const uint64_t vdesc0 = smem_desc(sbase + OFF_DEQ + DQ_VHI, ATOMC, 1024, kSwizzle128);
+  auto issue_qk = [&](int x) {
+    const uint32_t d = tmem + T_S + 64u * x;
+    const uint64_t kd = kdesc0 + static_cast<uint64_t>(x * (DEQ_BYTES >> 4));
+    if (leader) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t qa = qdesc0 + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          const uint64_t kb = kd + static_cast<uint64_t>((part * TILE + (kk >> 2) * ATOMC + (kk & 3) * 32) >> 4);
+          mma_ss(d, qa, kb, kIdescQK, (part | kk) != 0 ? 1u : 0u);
+        }
+    }
+  };
+  auto issue_pv = [&](int x) {
+    const uint32_t o = tmem + T_O + 128u * x;
+    const uint32_t p = tmem + T_S + 64u * x;
+    const uint64_t vd = vdesc0 + static_cast<uint64_t>(x * (DEQ_BYTES >> 4));
+    if (leader) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(o, p + 8u * kk, vd + static_cast<uint64_t>((part * TILE + kk * 2048) >> 4), kIdescPV, 1u);
+    }
+  };
+  auto commit = [&](int b) {
+    if (leader) mma_commit(bar(b));
+  };
+  bool ok = wait_bar(bar(B_QFULL), 0, ctl, budget, R_MMA, true);
+  if (ok) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (ok && u.T[x] > 0) {
+        ok = wait_bar(bar(B_KFULL + x), 0, ctl, budget, R_MMA, true);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(x);
+        commit(B_SFULL + x);
+        commit(B_KEMPTY + x);
+      }
+  }
+  for (int j = 0; ok && j < u.T[0]; ++j) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (j >= u.T[x]) continue;
+      const uint32_t par = static_cast<uint32_t>(j & 1);
+      if (!wait_bar(bar(B_VFULL + x), par, ctl, budget, R_MMA, true) ||
+          !wait_bar(bar(B_PFULL + x), par, ctl, budget, R_MMA, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv(x);
+      if (j == u.T[x] - 1) commit(B_ODONE + x);
+      commit(B_VEMPTY + x);
+      if (j + 1 < u.T[x]) {
+        if (!wait_bar(bar(B_KFULL + x), par ^ 1, ctl, budget, R_MMA, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_qk(x);
+        commit(B_SFULL + x);
+        commit(B_KEMPTY + x);
+      }
+    }
+  }
+  commit(B_DRAIN);
+  __syncwarp();
+  wait_bar(bar(B_DRAIN), 0, ctl, budget, R_DRAIN, false);
+}
+
+template <int O>
+__device__ __forceinline__ void ld32_at(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : Q8A_R8(r, O + 0), Q8A_R8(r, O + 8), Q8A_R8(r, O + 16), Q8A_R8(r, O + 24)
+      : "r"(taddr));
+}
+template <int O>
+__device__ __forceinline__ void wait_ld_at(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : Q8A_M8(r, O + 0), Q8A_M8(r, O + 8), Q8A_M8(r, O + 16), Q8A_M8(r, O + 24)::"memory");
+}
+
+// Rescale (or read) the 128 O columns of this thread's row in TMEM, 64 at a time.
+__device__ __forceinline__ void scale_o(uint32_t t_o, float alpha) {
+  const float2 al = make_float2(alpha, alpha);
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t o[64];
+    ld32_at<0>(t_o + 64 * hh, o);
+    ld32_at<32>(t_o + 64 * hh + 32, o);
+    wait_ld_at<0>(o);
+    wait_ld_at<32>(o);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al);
+      o[i] = __float_as_uint(v.x);
+      o[i + 1] = __float_as_uint(v.y);
+    }
+    tmem_st32_at<0>(t_o + 64 * hh, o);
+    tmem_st32_at<32>(t_o + 64 * hh + 32, o);
+  }
+}
+
+__device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x, uint8_t* smem,
+                                        uint32_t sbase, uint32_t tmem, Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  const int row = threadIdx.x & 127;
+  const int wq = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  const int T = u.T[x];
+  if (T == 0) return;
+  const int64_t rg = u.r0 + row;
+  const int64_t pos = a.q_pos0 + rg;
+  const bool active = rg < a.n_q && (!a.causal || pos >= a.kv_start);
+  const int64_t sidx = u.bh * a.n_q + rg;
+  const uint32_t t_s = tmem + lane_off + T_S + 64u * x;
+  const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
+  const bool fresh = x == 1;   // pipeline B starts empty; A merges it in at the end
+  const bool pair_merge = u.T[1] > 0;
+  float m_run = -INFINITY, l_run = 0.0f;
+  if (active && !fresh) {
+    m_run = a.m[sidx];
+    l_run = a.l[sidx];
+  }
+  {
+    uint32_t oh[64];
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      if (active && !fresh) {
+        const float4* src = reinterpret_cast<const float4*>(a.o + sidx * D + 64 * hh);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 p = src[i];
+          oh[4 * i + 0] = __float_as_uint(p.x);
+          oh[4 * i + 1] = __float_as_uint(p.y);
+          oh[4 * i + 2] = __float_as_uint(p.z);
+          oh[4 * i + 3] = __float_as_uint(p.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) oh[i] = 0u;
+      }
+      tmem_st32_at<0>(t_o + 64 * hh, oh);
+      tmem_st32_at<32>(t_o + 64 * hh + 32, oh);
+    }
+    tmem_wait_st();
+  }
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int64_t q_first = a.q_pos0 + u.r0;
+  bool ok = true;
+#pragma unroll 1
+  for (int t = 0; t < T; ++t) {
+    if (!wait_bar(bar(B_SFULL + x), t & 1, ctl, budget, R_SOFTMAX, true)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t s[64];
+    ld32_at<0>(t_s, s);
+    ld32_at<32>(t_s + 32, s);
+    wait_ld_at<0>(s);
+    wait_ld_at<32>(s);
+    const int64_t k0 = static_cast<int64_t>(2 * t + x) * BN;
+    const bool need_mask = (k0 + BN > a.kv_len) || (a.causal && a.kv_start + k0 + BN - 1 > q_first);
+    if (__builtin_expect(need_mask, 0)) {
+      int64_t lim = a.kv_len - 1 - k0;
+      if (a.causal) lim = i64min(lim, pos - a.kv_start - k0);
+      const int li = static_cast<int>(i64max(-1, i64min(lim, BN - 1)));
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (j > li) s[j] = __float_as_uint(-INFINITY);
+    }
+    float pm[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pm[i] = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < 32; ++p)
+      pm[p & 3] = max3(pm[p & 3], __uint_as_float(s[2 * p]), __uint_as_float(s[2 * p + 1]));
+    const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+    const float t_nat = mx * a.scale;
+    float alpha = 1.0f;
+    const bool resc = t_nat > m_run;
+    if (resc) {
+      alpha = (m_run == -INFINITY) ? 0.0f : ex2_approx((m_run - t_nat) * kLog2e);
+      m_run = t_nat;
+    }
+    const float mlog = (m_run == -INFINITY) ? 0.0f : m_run * kLog2e;
+    const float2 nm2 = make_float2(-mlog, -mlog);
+    float2 rs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.0f, 0.0f);
+    uint32_t p[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float2 sv = make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+      const float2 e = __ffma2_rn(sv, sl2, nm2);
+      const float2 bt = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+      rs[i & 3] = __fadd2_rn(rs[i & 3], bt);
+      p[i] = pack_half2(bt.x, bt.y);
+    }
+    tmem_st32(t_s, p);
+    // PV_x(t-1) has completed (QK_x(t), issued after it, has): O is stable
+    if (__any_sync(0xFFFFFFFFu, resc)) scale_o(t_o, alpha);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar(B_PFULL + x));
+    const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+    l_run = fmaf(l_run, alpha, r.x + r.y);
+  }
+  float4* xch = reinterpret_cast<float4*>(smem + OFF_XCH) + row;
+  if (pair_merge && x == 1) {
+    *xch = make_float4(m_run, l_run, ok ? 1.0f : 0.0f, 0.0f);
+    mbar_arrive(bar(B_MERGE));
+    return;
+  }
+  if (!ok) return;
+  if (!wait_bar(bar(B_ODONE + x), 0, ctl, budget, R_SOFTMAX, true)) return;
+  tc_fence_after();
+  float m_b = -INFINITY, l_b = 0.0f;
+  if (pair_merge) {
+    if (!wait_bar(bar(B_MERGE), 0, ctl, budget, R_SOFTMAX, true) ||
+        !wait_bar(bar(B_ODONE + 1), 0, ctl, budget, R_SOFTMAX, true))
+      return;
+    tc_fence_after();
+    const float4 pb = *xch;
+    if (pb.z == 0.0f) return;   // pipeline B gave up; the failure is already recorded
+    m_b = pb.x;
+    l_b = pb.y;
+  }
+  // the chunk recurrence over the two partial states (B's weight is 0 when
+  // it holds no key); the weight of the larger max is exactly 1
+  const float m = fmaxf(m_run, m_b);
+  const float wa = (m_run == m) ? 1.0f : (m_run == -INFINITY ? 0.0f : ex2_approx((m_run - m) * kLog2e));
+  const float wb = (m_b == m) ? 1.0f : (m_b == -INFINITY ? 0.0f : ex2_approx((m_b - m) * kLog2e));
+  if (active) {
+    a.m[sidx] = m;
+    a.l[sidx] = pair_merge ? fmaf(wa, l_run, wb * l_b) : l_run;
+  }
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {   // 32 channels at a time
+    uint32_t oa[32], ob[32];
+    tmem_ld32(t_o + 32 * q, oa);
+    if (pair_merge) tmem_ld32(t_o + 128 + 32 * q, ob);
+    tmem_wait_ld(oa);
+    if (pair_merge) tmem_wait_ld(ob);
+    if (active) {
+      float4* dst = reinterpret_cast<float4*>(a.o + sidx * D + 32 * q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * i + e;
+          v[e] = pair_merge ? fmaf(wa, __uint_as_float(oa[c]), wb * __uint_as_float(ob[c]))
+                            : __uint_as_float(oa[c]);
+        }
+        dst[i] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_step_d128_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + OFF_CTL);
+  const int warp = threadIdx.x >> 5;
+  const int wg = warp >> 2;
+  const Unit u = make_unit(a);
+  if (u.T_all == 0) return;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBAR; ++i) {
+      uint32_t count = 1;
+      if (i >= B_RAWEMPTY && i < B_RAWEMPTY + NR) count = 128;   // every dequant thread
+      if (i >= B_KFULL && i < B_KFULL + 2) count = 64;           // the K threads
+      if (i >= B_VFULL && i < B_VFULL + 2) count = 64;           // the V threads
+      if (i >= B_PFULL && i < B_PFULL + 2) count = 128;          // softmax threads of a pipeline
+      if (i == B_MERGE) count = 128;                             // softmax threads of pipeline B
+      mbar_init(sbase + OFF_BAR + 8u * i, count);
+    }
+    ctl->abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(sbase + OFF_CTL, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  if (wg < 2) {
+    reg_alloc<kRegSoftmax>();
+    softmax(a, u, wg, smem, sbase, tmem, ctl);
+  } else {
+    reg_dealloc<kRegOther>();
+    if (wg == 2) {
+      dequant(a, u, smem, sbase, ctl);
+    } else if (warp == 12) {
+      producer(&qmap, a, u, smem, sbase, ctl);
+    } else if (warp == 13) {
+      mma(a, u, sbase, tmem, ctl);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace d128
+
 }  // namespace
 
 cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream) {
@@ -940,6 +1483,38 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
   if (e != cudaSuccess)
     set_launch_note("chunk_step_kernel<<<(%lld, %u), %d, %d>>>", static_cast<long long>(blocks), gy,
                     kThreads, SMEM_BYTES);
+  return e;
+}
+
+cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(d128::chunk_step_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             d128::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, d128::chunk_step_d128_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * d128::kThreads != 65536 || fa.maxThreadsPerBlock < d128::kThreads) {
+      set_launch_note("chunk_step_d128_kernel has %d registers per thread and at most %d threads per "
+                      "block; the register split needs %d and %d",
+                      fa.numRegs, fa.maxThreadsPerBlock, 65536 / d128::kThreads, d128::kThreads);
+      return cudaErrorInvalidConfiguration;
+    }
+    configured_device = dev;
+  }
+  const int64_t blocks = static_cast<int64_t>(args.n_qtiles) * args.bh;   // one 128-row tile each
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  d128::chunk_step_d128_kernel<<<static_cast<unsigned>(blocks), d128::kThreads, d128::SMEM_BYTES, stream>>>(
+      qmap, args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess)
+    set_launch_note("chunk_step_d128_kernel<<<%lld, %d, %d>>>", static_cast<long long>(blocks),
+                    d128::kThreads, d128::SMEM_BYTES);
   return e;
 }
 

@@ -23,20 +23,23 @@ struct NvtxRange {
 constexpr int kHeadDim = 64;
 constexpr int kRowBytes = 68;  // one head row: two 34-byte Q8_0 blocks
 
-// q8kv_quantize: fp32 [B][M][H][64] -> Q8_0 planes [B][H] of 68-byte rows.
+// q8kv_quantize: fp32 [B][M][H][D] -> Q8_0 planes [B][H] of D/32*34-byte rows
+// (D = head_dim, 64 or 128).
 cudaError_t launch_quantize(const float* x, uint8_t* out, int64_t batch, int64_t n_tokens,
-                            int32_t heads, int64_t plane_stride, cudaStream_t stream);
+                            int32_t heads, int32_t head_dim, int64_t plane_stride,
+                            cudaStream_t stream);
 
-// attn_state_init over `rows` = B*H*n_q state rows.
-cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, cudaStream_t stream);
+// attn_state_init over `rows` = B*H*n_q state rows of head_dim O channels.
+cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, int32_t head_dim,
+                              cudaStream_t stream);
 
-// attn_finalize: fp32 O, l -> fp16 out [B][n_q][H][64].
+// attn_finalize: fp32 O, l -> fp16 out [B][n_q][H][D].
 cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
-                            int32_t heads, int64_t n_q, cudaStream_t stream);
+                            int32_t heads, int64_t n_q, int32_t head_dim, cudaStream_t stream);
 // The same for query rows row0 .. row0+n_rows-1 of every (b, h) plane only.
 cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int64_t batch,
-                                 int32_t heads, int64_t n_q, int64_t row0, int64_t n_rows,
-                                 cudaStream_t stream);
+                                 int32_t heads, int64_t n_q, int32_t head_dim, int64_t row0,
+                                 int64_t n_rows, cudaStream_t stream);
 
 // Arguments of one chunk-step launch (everything but the Q tensor map).
 struct ChunkArgs {
@@ -59,6 +62,7 @@ struct ChunkArgs {
   float scale_log2;       // scale * log2(e)
   int32_t causal;
   int32_t inject;         // test hook: 1 = first block skips its query-tile load
+  int32_t head_dim;       // 64 or 128
   int32_t pair;           // 1: one query tile, no causal mask -- the CTA's two softmax
                           // pipelines share the rows and split the key tiles (even / odd)
   uint64_t timeout_ns;    // budget of every device-side wait
@@ -76,6 +80,11 @@ struct ChunkArgs {
 // The tensor map must describe Q as fp16 {H*64, n_q, B} with a {64, 128, 1}
 // box and 128-byte swizzle.
 cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
+
+// The head_dim 128 chunk step: Q as fp16 {H*128, n_q, B} with a {64, 128, 1}
+// box and 128-byte swizzle; n_qtiles counts 128-row query tiles (one per CTA);
+// no split form.
+cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
 
 // Record `msg` as the calling thread's last error (q8a_last_error) and return code.
 int set_error(int code, const char* fn, const char* msg);

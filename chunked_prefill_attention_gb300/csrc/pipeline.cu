@@ -158,7 +158,8 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
                               s0, n, m, l, o, batch, heads, n_tokens, head_dim, scale, causal, cs)) != Q8A_OK)
       return bail(rc);
     if (causal) {
-      if ((e = q8a::launch_finalize_rows(l, o, out_dev, batch, heads, n_tokens, s0, n, cs)) != cudaSuccess)
+      if ((e = q8a::launch_finalize_rows(l, o, out_dev, batch, heads, n_tokens, head_dim, s0, n, cs)) !=
+          cudaSuccess)
         return bail(cuda_err(e, "finalize of a row block"));
       if ((e = cudaEventRecord(ev_fin, cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
       prev_r0 = s0;

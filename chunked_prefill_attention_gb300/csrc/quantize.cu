@@ -15,13 +15,13 @@
 // division).  The theorem needs a normal quotient; a quotient below 2^-126 is
 // far below 0.5 and rounds to code 0 either way.
 //
-// Memory plan (HBM-bound: 256 B read + 68 B written per 64-value head row):
-// one block handles 16 tokens x 8 heads, one warp per head and one thread per
-// 32-value block (lane 2t + j: token t, block j).  A thread loads its block's
+// Memory plan (HBM-bound: 4 B read per value + 34 B written per 32 values):
+// one block handles 16 tokens (8 at head_dim 128) x 8 heads, one warp per head
+// and one thread per 32-value block.  A thread loads its block's
 // 128 contiguous bytes with four 256-bit loads (eight 128-bit loads when x is
 // only 16-byte aligned), reduces amax in registers, forms d and the reciprocal
 // once, and emits its 32 codes as eight 32-bit words into its head's staging
-// rows in shared memory.  The warp then writes its head's 16 consecutive rows
+// rows in shared memory.  The warp then writes its head's consecutive rows
 // (1088 contiguous, 16-byte-aligned bytes of the head-major plane) back with
 // 128-bit stores (32-bit stores for a ragged last tile); no block-wide barrier,
 // so the warps of a block load, convert and store independently.
@@ -35,10 +35,10 @@
 namespace q8a {
 namespace {
 
-constexpr int kTok = 16;    // tokens per block
-constexpr int kHeads = 8;   // heads per block
-constexpr int kThreads = 256;   // two per head row
-static_assert(kThreads == 2 * kTok * kHeads, "one thread per 32-value block");
+constexpr int kHeads = 8;       // heads per block, one warp each
+constexpr int kThreads = 256;
+static_assert(kThreads / 32 == kHeads, "one warp per head of the block");
+constexpr int kStageBytes = 1088;   // one head's rows of a tile: 16 x 68 or 8 x 136 bytes
 
 // RN(x / d) for d > 0, from y = RN(1 / d) (see the note above).
 __device__ __forceinline__ float div_rn_by(float x, float d, float y) {
@@ -65,13 +65,20 @@ __device__ __forceinline__ void ldg256(const float* p, float* v) {
                : "l"(p));
 }
 
+// kD: channels per head row (64 or 128: kD / 32 Q8_0 blocks, kD / 32 * 34
+// bytes per row).  A warp quantises kTok = 32 / blocks consecutive tokens of one
+// head, one lane per block (lane = blocks * token + block).
 // kWide: x is 32-byte aligned and every block is loaded with 256-bit loads
 // (every block starts a multiple of 128 bytes after x); otherwise 128-bit loads.
-template <bool kWide>
+template <int kD, bool kWide>
 __global__ void __launch_bounds__(kThreads)
 q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t n_tokens,
                      int32_t heads, int64_t plane_stride, int32_t tok_tiles, int32_t head_tiles) {
-  __shared__ __align__(16) uint8_t stage[kHeads][kTok * kRowBytes];
+  constexpr int kBlk = kD / 32;
+  constexpr int kRow = kBlk * 34;
+  constexpr int kTok = 32 / kBlk;
+  static_assert(kTok * kRow == kStageBytes, "staging rows of one head");
+  __shared__ __align__(16) uint8_t stage[kHeads][kStageBytes];
 
   const int64_t blk = blockIdx.x;
   const int ht = static_cast<int>(blk % head_tiles);
@@ -86,11 +93,11 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   // warp -> head hh of the tile; lane -> (token tok, 32-value block bb)
   const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (hh >= n_h) return;
-  const int tok = lane >> 1, bb = lane & 1;
+  const int tok = lane / kBlk, bb = lane % kBlk;
   const bool valid = tok < n_tok;
   float v[32];
   if (valid) {
-    const float* src = x + (((b * n_tokens + t0 + tok) * heads + h0 + hh) * kHeadDim + 32 * bb);
+    const float* src = x + (((b * n_tokens + t0 + tok) * heads + h0 + hh) * kD + 32 * bb);
     if (kWide) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) ldg256(src + 8 * i, v + 8 * i);
@@ -123,17 +130,19 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
            (code8(v[4 * k + 3], d, y, finite_nonzero) << 24);
   const uint32_t dbits = __half_as_ushort(d16);
   if (valid) {
-    // row bytes: block 0 = d at 0, codes at 2..33; block 1 = d at 34, codes at 36..67
-    uint8_t* row = &stage[hh][tok * kRowBytes];   // 4-byte aligned (68-byte rows)
-    if (bb == 0) {
-      uint32_t* p = reinterpret_cast<uint32_t*>(row);
+    // block bb of the row: d at 34 * bb, codes at 34 * bb + 2.  Rows start
+    // 4-byte aligned; an even block starts 4-byte aligned (codes at 2 mod 4),
+    // an odd one 2 mod 4 (codes 4-byte aligned).
+    uint8_t* blk_at = &stage[hh][tok * kRow + 34 * bb];
+    if ((bb & 1) == 0) {
+      uint32_t* p = reinterpret_cast<uint32_t*>(blk_at);
       p[0] = dbits | (w[0] << 16);
 #pragma unroll
       for (int k = 0; k < 7; ++k) p[1 + k] = __funnelshift_r(w[k], w[k + 1], 16);
-      *reinterpret_cast<uint16_t*>(row + 32) = static_cast<uint16_t>(w[7] >> 16);
+      *reinterpret_cast<uint16_t*>(blk_at + 32) = static_cast<uint16_t>(w[7] >> 16);
     } else {
-      *reinterpret_cast<uint16_t*>(row + 34) = static_cast<uint16_t>(dbits);
-      uint32_t* p = reinterpret_cast<uint32_t*>(row + 36);
+      *reinterpret_cast<uint16_t*>(blk_at) = static_cast<uint16_t>(dbits);
+      uint32_t* p = reinterpret_cast<uint32_t*>(blk_at + 2);
 #pragma unroll
       for (int k = 0; k < 8; ++k) p[k] = w[k];
     }
@@ -141,35 +150,44 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   __syncwarp();
 
   // Write back: head hh's rows t0 .. t0+n_tok-1 are contiguous in its plane
-  // (byte t0 * 68 = tt * 1088, a multiple of 16).
-  static_assert(kThreads / 32 == kHeads && 2 * kTok == 32, "one warp per head, two lanes per token");
-  uint8_t* dst = out + (b * heads + h0 + hh) * plane_stride + t0 * kRowBytes;
+  // (byte t0 * kRow = tt * 1088, a multiple of 16).
+  uint8_t* dst = out + (b * heads + h0 + hh) * plane_stride + t0 * kRow;
   if (n_tok == kTok) {
     const uint4* s4 = reinterpret_cast<const uint4*>(stage[hh]);
     uint4* d4 = reinterpret_cast<uint4*>(dst);
-    for (int i = lane; i < kTok * kRowBytes / 16; i += 32) d4[i] = s4[i];
+    for (int i = lane; i < kStageBytes / 16; i += 32) d4[i] = s4[i];
   } else {
     const uint32_t* s1 = reinterpret_cast<const uint32_t*>(stage[hh]);
     uint32_t* d1 = reinterpret_cast<uint32_t*>(dst);
-    for (int i = lane; i < n_tok * (kRowBytes / 4); i += 32) d1[i] = s1[i];
+    for (int i = lane; i < n_tok * (kRow / 4); i += 32) d1[i] = s1[i];
   }
 }
 
-}  // namespace
-
-cudaError_t launch_quantize(const float* x, uint8_t* out, int64_t batch, int64_t n_tokens,
-                            int32_t heads, int64_t plane_stride, cudaStream_t stream) {
+template <int kD>
+cudaError_t launch_quantize_d(const float* x, uint8_t* out, int64_t batch, int64_t n_tokens,
+                              int32_t heads, int64_t plane_stride, cudaStream_t stream) {
+  constexpr int kTok = 32 / (kD / 32);
   const int64_t tok_tiles = (n_tokens + kTok - 1) / kTok;
   const int64_t head_tiles = (heads + kHeads - 1) / kHeads;
   const int64_t blocks = batch * tok_tiles * head_tiles;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF || tok_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const bool wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0;
-  auto kernel = wide ? q8kv_quantize_kernel<true> : q8kv_quantize_kernel<false>;
+  auto kernel = wide ? q8kv_quantize_kernel<kD, true> : q8kv_quantize_kernel<kD, false>;
   kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
       x, out, n_tokens, heads, plane_stride, static_cast<int32_t>(tok_tiles),
       static_cast<int32_t>(head_tiles));
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* x, uint8_t* out, int64_t batch, int64_t n_tokens,
+                            int32_t heads, int32_t head_dim, int64_t plane_stride,
+                            cudaStream_t stream) {
+  if (head_dim == 64) return launch_quantize_d<64>(x, out, batch, n_tokens, heads, plane_stride, stream);
+  if (head_dim == 128) return launch_quantize_d<128>(x, out, batch, n_tokens, heads, plane_stride, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace q8a

@@ -3,11 +3,11 @@
 // Speculative Decode (1M Context)", §3: m, l, O kept in global memory between
 // chunks; Attention_i = O_i / l_i after chunk C-1).
 //
-// Both kernels are HBM streams: init writes 264 B per (row, head); finalise
-// reads 260 B and writes 128 B.  Finalise maps 8 threads to one 64-float O row
-// (two 128-bit loads each) and writes 8 fp16 (one 128-bit store) per thread, so
-// both the head-major fp32 reads and the token-major fp16 writes are whole
-// 128-byte lines.
+// Both kernels are HBM streams: init writes 4 * (2 + D) B per (row, head)
+// (264 B at head_dim 64); finalise reads 4 * (1 + D) B and writes 2 * D B.
+// Finalise maps D / 8 threads to one D-float O row (two 128-bit loads each) and
+// writes 8 fp16 (one 128-bit store) per thread, so both the head-major fp32
+// reads and the token-major fp16 writes are whole 128-byte lines.
 
 #include <cuda_fp16.h>
 
@@ -22,34 +22,37 @@ __host__ __device__ __forceinline__ int64_t i64min_host(int64_t a, int64_t b) { 
 
 __global__ void __launch_bounds__(kThreads)
 state_init_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
-                  int64_t rows) {
+                  int64_t rows, int32_t head_dim) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   const int64_t start = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t i = start; i < rows * (kHeadDim / 4); i += stride) o[i] = z;
+  for (int64_t i = start; i < rows * (head_dim / 4); i += stride) o[i] = z;
   for (int64_t i = start; i < rows; i += stride) {
     m[i] = -INFINITY;
     l[i] = 0.0f;
   }
 }
 
+// kD / 8 threads per state row, 8 channels each.
+template <int kD>
 __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4* __restrict__ out,
                 int64_t n_q, int32_t heads, int64_t row0, int64_t n_rows, int64_t rows) {
   // rows = B*H*n_rows state rows: query rows row0 .. row0+n_rows-1 of every plane
+  constexpr int kParts = kD / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * 8;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * kParts;
        g += stride) {
-    const int64_t k = g >> 3;           // (b*H + h)*n_rows + (r - row0)
-    const int part = static_cast<int>(g & 7);
+    const int64_t k = g / kParts;       // (b*H + h)*n_rows + (r - row0)
+    const int part = static_cast<int>(g % kParts);
     const int64_t r = row0 + k % n_rows;
     const int64_t bh = k / n_rows;
     const int64_t row = bh * n_q + r;   // (b*H + h)*n_q + r
     const int64_t h = bh % heads;
     const int64_t b = bh / heads;
     const float lv = __ldg(l + row);
-    const float4 a = __ldg(o + row * 16 + 2 * part);
-    const float4 c = __ldg(o + row * 16 + 2 * part + 1);
+    const float4 a = __ldg(o + row * (kD / 4) + 2 * part);
+    const float4 c = __ldg(o + row * (kD / 4) + 2 * part + 1);
     float y[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) y[i] = (lv > 0.0f) ? __fdiv_rn(y[i], lv) : 0.0f;
@@ -62,7 +65,7 @@ finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4
     pk.y = *reinterpret_cast<uint32_t*>(&h1);
     pk.z = *reinterpret_cast<uint32_t*>(&h2);
     pk.w = *reinterpret_cast<uint32_t*>(&h3);
-    out[((b * n_q + r) * heads + h) * 8 + part] = pk;
+    out[((b * n_q + r) * heads + h) * kParts + part] = pk;
   }
 }
 
@@ -133,24 +136,27 @@ int grid_for(int64_t work) {
 
 }  // namespace
 
-cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, cudaStream_t stream) {
+cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, int32_t head_dim,
+                              cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  state_init_kernel<<<grid_for(rows * 16), kThreads, 0, stream>>>(m, l, reinterpret_cast<float4*>(o),
-                                                                  rows);
+  state_init_kernel<<<grid_for(rows * (head_dim / 4)), kThreads, 0, stream>>>(
+      m, l, reinterpret_cast<float4*>(o), rows, head_dim);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
-                            int32_t heads, int64_t n_q, cudaStream_t stream) {
-  return launch_finalize_rows(l, o, out, batch, heads, n_q, 0, n_q, stream);
+                            int32_t heads, int64_t n_q, int32_t head_dim, cudaStream_t stream) {
+  return launch_finalize_rows(l, o, out, batch, heads, n_q, head_dim, 0, n_q, stream);
 }
 
 cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int64_t batch,
-                                 int32_t heads, int64_t n_q, int64_t row0, int64_t n_rows,
-                                 cudaStream_t stream) {
+                                 int32_t heads, int64_t n_q, int32_t head_dim, int64_t row0,
+                                 int64_t n_rows, cudaStream_t stream) {
   const int64_t rows = batch * heads * n_rows;
   if (rows <= 0) return cudaSuccess;
-  finalize_kernel<<<grid_for(rows * 8), kThreads, 0, stream>>>(
+  if (head_dim != 64 && head_dim != 128) return cudaErrorInvalidValue;
+  auto kernel = head_dim == 64 ? finalize_kernel<64> : finalize_kernel<128>;
+  kernel<<<grid_for(rows * (head_dim / 8)), kThreads, 0, stream>>>(
       l, reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, row0,
       n_rows, rows);
   return cudaGetLastError();

@@ -34,6 +34,7 @@ SIGNATURES = {
     "q8a_abi_version": (_U32, []),
     "q8a_last_error": (ctypes.c_char_p, []),
     "q8a_plane_stride_bytes": (_I64, [_I64]),
+    "q8a_plane_stride_bytes_for": (_I64, [_I64, _I32]),
     "q8kv_quantize": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _I32, _I64, _P]),
     "attn_state_init": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I64, _I32, _P]),
     "attn_chunk_step": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32,
@@ -93,15 +94,21 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def plane_stride(n_tokens):
-    return int(load().q8a_plane_stride_bytes(n_tokens))
+def row_bytes(head_dim):
+    """Bytes of one Q8_0 head row: head_dim / 32 blocks of 34 bytes."""
+    return head_dim // 32 * 34
+
+
+def plane_stride(n_tokens, head_dim=HEAD_DIM):
+    return int(load().q8a_plane_stride_bytes_for(n_tokens, head_dim))
 
 
 def q8kv_quantize(x, out=None, stride=None):
-    """x: fp32 CUDA [B, M, H, 64] -> uint8 [B, H, stride] Q8_0 planes (rows of 68 B)."""
+    """x: fp32 CUDA [B, M, H, D] (D = 64 or 128) -> uint8 [B, H, stride] Q8_0
+    planes (rows of D/32*34 B)."""
     B, M, H, D = x.shape
     if stride is None:
-        stride = plane_stride(M)
+        stride = plane_stride(M, D)
     if out is None:
         out = torch.empty((B, H, stride), dtype=torch.uint8, device=x.device)
     _check(load().q8kv_quantize(_ptr(x), _ptr(out), B, M, H, D, stride, _stream(x)))
@@ -109,12 +116,12 @@ def q8kv_quantize(x, out=None, stride=None):
 
 
 class State:
-    """Persistent per-row online-softmax state (fp32): m, l [B, H, n_q]; O [B, H, n_q, 64]."""
+    """Persistent per-row online-softmax state (fp32): m, l [B, H, n_q]; O [B, H, n_q, D]."""
 
-    def __init__(self, batch, heads, n_q, device, init=True):
+    def __init__(self, batch, heads, n_q, device, init=True, head_dim=HEAD_DIM):
         self.m = torch.empty((batch, heads, n_q), dtype=torch.float32, device=device)
         self.l = torch.empty((batch, heads, n_q), dtype=torch.float32, device=device)
-        self.o = torch.empty((batch, heads, n_q, HEAD_DIM), dtype=torch.float32, device=device)
+        self.o = torch.empty((batch, heads, n_q, head_dim), dtype=torch.float32, device=device)
         if init:
             attn_state_init(self)
 
@@ -122,10 +129,14 @@ class State:
     def shape(self):
         return self.m.shape
 
+    @property
+    def head_dim(self):
+        return self.o.shape[-1]
+
 
 def attn_state_init(state):
     B, H, n = state.shape
-    _check(load().attn_state_init(_ptr(state.m), _ptr(state.l), _ptr(state.o), B, H, n, HEAD_DIM,
+    _check(load().attn_state_init(_ptr(state.m), _ptr(state.l), _ptr(state.o), B, H, n, state.head_dim,
                                   _stream(state.m)))
     return state
 
@@ -134,9 +145,9 @@ def attn_chunk_step(q, k8, v8, kv_start, kv_len, state, q_pos0=0, scale=None, ca
                     stride=None, k_offset_bytes=0):
     """Fold KV keys [kv_start, kv_start + kv_len) into `state`.
 
-    q: fp16 [B, n_q, H, 64]; k8, v8: uint8 Q8_0 planes [B, H, stride] whose byte
+    q: fp16 [B, n_q, H, D]; k8, v8: uint8 Q8_0 planes [B, H, stride] whose byte
     `k_offset_bytes` is the chunk's key 0 (so a whole-sequence buffer is passed
-    with k_offset_bytes = kv_start * 68)."""
+    with k_offset_bytes = kv_start * row_bytes(D))."""
     B, n_q, H, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -202,11 +213,11 @@ def attn_chunk_step_split(q, k8, v8, kv_start, kv_len, state, split_keys, worksp
 
 
 def attn_finalize(state, out=None):
-    """O / l -> fp16 [B, n_q, H, 64]."""
+    """O / l -> fp16 [B, n_q, H, D]."""
     B, H, n = state.shape
     if out is None:
-        out = torch.empty((B, n, H, HEAD_DIM), dtype=torch.float16, device=state.m.device)
-    _check(load().attn_finalize(_ptr(state.l), _ptr(state.o), _ptr(out), B, H, n, HEAD_DIM,
+        out = torch.empty((B, n, H, state.head_dim), dtype=torch.float16, device=state.m.device)
+    _check(load().attn_finalize(_ptr(state.l), _ptr(state.o), _ptr(out), B, H, n, state.head_dim,
                                 _stream(state.m)))
     return out
 
@@ -218,13 +229,13 @@ def prefill_attention(q, k, v, chunk, scale=None, causal=True, k8=None, v8=None,
     k8 = q8kv_quantize(k, k8)
     v8 = q8kv_quantize(v, v8)
     if state is None:
-        state = State(B, H, M, q.device, init=True)
+        state = State(B, H, M, q.device, init=True, head_dim=D)
     else:
         attn_state_init(state)
     for s0 in range(0, M, chunk):
         n = min(chunk, M - s0)
         attn_chunk_step(q, k8, v8, s0, n, state, scale=scale, causal=causal,
-                        k_offset_bytes=s0 * ROW_BYTES)
+                        k_offset_bytes=s0 * row_bytes(D))
     out = attn_finalize(state, out)
     return out, k8, v8
 

@@ -14,6 +14,10 @@ dimension 64 and a causal mask, computed chunk by chunk over the KV:
   m64k       1 x 65536      8192       as m512                                  (3)
   m1m        1 x 1048576    131072     as m512                                  (4)
 
+and one head_dim 128 problem (an extension beyond the pages' head_dim 64):
+
+  m16k_d128  1 x 16384      4096       32 heads x 128, as m512                  (6)
+
 The pages measure no public dataset; these draws stand in for the activations
 of a prefill pass.  Inputs are drawn with a torch generator on the device they
 are created on, in the fixed order Q, then K, then V.
@@ -73,6 +77,7 @@ WORKLOADS = {
         Workload("b8_m2k", 8, 2048, 512, 2, kv_sigma=0.5),
         Workload("m64k", 1, 65536, 8192, 3),
         Workload("m1m", 1, 1048576, 131072, 4),
+        Workload("m16k_d128", 1, 16384, 4096, 6, head_dim=128),
     ]
 }
 

@@ -23,17 +23,21 @@
  *     thread-local message for the last failing call of the calling thread.
  *   - Sizes of zero are allowed and make the call a no-op; negative sizes are
  *     Q8A_ERR_INVALID_ARG.
- *   - head_dim must be 64 (two Q8_0 blocks per head row).
+ *   - head_dim D is 64 (two Q8_0 blocks per head row) for every call, and
+ *     128 (four blocks) for q8kv_quantize, attn_state_init, attn_chunk_step,
+ *     attn_chunk_step_gqa and attn_finalize; the split, allocation-free split
+ *     and pipelined calls answer Q8A_ERR_UNSUPPORTED for 128.
  *   - Layouts (all row-major, contiguous):
- *       Q, out    fp16  [B][n_q][H][64]          token-major
- *       x (K, V)  fp32  [B][n_tokens][H][64]     token-major
- *       K8, V8    Q8_0  [B][H] planes of n_tokens rows of 68 bytes; plane
- *                 (b, h) starts `plane_stride_bytes * (b*H + h)` bytes after
- *                 the base.  One 68-byte row = block 0 (channels 0..31) then
- *                 block 1 (channels 32..63); each 34-byte block is an fp16
- *                 scale d (little-endian) followed by 32 int8 codes.
+ *       Q, out    fp16  [B][n_q][H][D]           token-major
+ *       x (K, V)  fp32  [B][n_tokens][H][D]      token-major
+ *       K8, V8    Q8_0  [B][H] planes of n_tokens rows of D/32*34 bytes (68 at
+ *                 D = 64, 136 at D = 128); plane (b, h) starts
+ *                 `plane_stride_bytes * (b*H + h)` bytes after the base.  A row
+ *                 is block 0 (channels 0..31), block 1 (32..63), ...; each
+ *                 34-byte block is an fp16 scale d (little-endian) followed by
+ *                 32 int8 codes.
  *       m, l      fp32  [B][H][n_q]
- *       O         fp32  [B][H][n_q][64]
+ *       O         fp32  [B][H][n_q][D]
  *   - Device wait budget: every wait inside a kernel is bounded (default 2 s,
  *     see q8a_set_wait_timeout_ns).  A wait that runs out stops the kernel's
  *     blocks cleanly and records Q8A_ERR_TIMEOUT in a per-device status word
@@ -51,20 +55,21 @@ extern "C" {
 
 /* Raised whenever an entry point is added or its contract changes.  2: the
  * split, allocation-free split, pipelined and grouped-query calls.  3: the
- * pipelined call streams K and V through two chunk slots (kv_slots). */
-#define Q8A_ABI_VERSION 3u
+ * pipelined call streams K and V through two chunk slots (kv_slots).  4:
+ * head_dim 128 and q8a_plane_stride_bytes_for. */
+#define Q8A_ABI_VERSION 4u
 
 enum {
   Q8A_OK = 0,
   Q8A_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad stride or shape */
   Q8A_ERR_MISALIGNED = -2,  /* a pointer or stride lacks the required alignment */
-  Q8A_ERR_UNSUPPORTED = -3, /* head_dim other than 64, or a size beyond int32 tiles */
+  Q8A_ERR_UNSUPPORTED = -3, /* a head_dim the call does not support, or a size beyond int32 tiles */
   Q8A_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
   Q8A_ERR_TIMEOUT = -5      /* a device-side wait ran out of budget */
 };
 
 #define Q8A_ROW_BYTES 68 /* one 64-channel head row: two 34-byte Q8_0 blocks */
-#define Q8A_HEAD_DIM 64  /* the supported head dimension */
+#define Q8A_HEAD_DIM 64  /* the head dimension every call supports */
 
 /* ABI version of the loaded library (Q8A_ABI_VERSION). */
 uint32_t q8a_abi_version(void);
@@ -74,6 +79,10 @@ const char *q8a_last_error(void);
 
 /* Smallest valid plane stride for n_tokens rows: n_tokens*68 rounded up to 16. */
 int64_t q8a_plane_stride_bytes(int64_t n_tokens);
+
+/* The same for head_dim 64 or 128: n_tokens * head_dim/32*34 rounded up to 16;
+ * -1 for a negative n_tokens or another head_dim. */
+int64_t q8a_plane_stride_bytes_for(int64_t n_tokens, int32_t head_dim);
 
 /*
  * q8kv_quantize -- dynamic Q8_0 quantisation of one K or V tensor [ARCH].
@@ -85,10 +94,10 @@ int64_t q8a_plane_stride_bytes(int64_t n_tokens);
  * The result is bit-exact and deterministic.  Inputs must be finite with
  * |x| <= 65504*127 (larger values are not detected).
  *
- *   x                  fp32 [B][n_tokens][H][64], 16-byte aligned.
+ *   x                  fp32 [B][n_tokens][H][D], 16-byte aligned.
  *   q8_out             Q8_0 planes [B][H], row t of plane (b,h) at byte
- *                      plane_stride*(b*H+h) + 68*t; 16-byte aligned.
- *   out_plane_stride_bytes  >= n_tokens*68 and a multiple of 16.
+ *                      plane_stride*(b*H+h) + (D/32*34)*t; 16-byte aligned.
+ *   out_plane_stride_bytes  >= n_tokens*D/32*34 and a multiple of 16.
  * Errors: Q8A_ERR_INVALID_ARG, Q8A_ERR_MISALIGNED, Q8A_ERR_UNSUPPORTED, Q8A_ERR_CUDA.
  */
 int q8kv_quantize(const float *x, void *q8_out, int64_t batch, int64_t n_tokens,
@@ -98,7 +107,7 @@ int q8kv_quantize(const float *x, void *q8_out, int64_t batch, int64_t n_tokens,
 /*
  * attn_state_init -- the persistent per-row state before the first chunk
  * [STREAM §3]: m_i = -inf, l_i = 0, O_i = 0 for every (b, h, row).
- *   m, l  fp32 [B][H][n_q] (4-byte aligned);  o fp32 [B][H][n_q][64] (16-byte aligned).
+ *   m, l  fp32 [B][H][n_q] (4-byte aligned);  o fp32 [B][H][n_q][D] (16-byte aligned).
  */
 int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
                     int64_t n_q, int32_t head_dim, void *stream);
@@ -116,13 +125,14 @@ int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
  * ([ARCH] causal skipping).  Chunks may be folded in any order; the result is
  * the same up to floating-point rounding.
  *
- *   q            fp16 [B][n_q][H][64], 16-byte aligned (rows of this call's queries).
+ *   q            fp16 [B][n_q][H][D], 16-byte aligned (rows of this call's queries).
  *   k_q8, v_q8   key 0 of this chunk in plane (b=0, h=0); plane (b,h) starts
  *                kv_plane_stride_bytes*(b*H+h) later; 16-byte aligned.
- *   kv_plane_stride_bytes  >= kv_len*68 and a multiple of 16.  (A slice of a
- *                whole-sequence Q8_0 buffer uses that buffer's stride and a
- *                pointer advanced by kv_start*68 bytes, which is 16-byte aligned
- *                when kv_start is a multiple of 4.)
+ *   kv_plane_stride_bytes  >= kv_len*D/32*34 and a multiple of 16.  (A slice of
+ *                a whole-sequence Q8_0 buffer uses that buffer's stride and a
+ *                pointer advanced by kv_start*D/32*34 bytes, which is 16-byte
+ *                aligned when kv_start is a multiple of 4 at D = 64, of 2 at
+ *                D = 128.)
  *   kv_start     absolute position of the chunk's first key (>= 0).
  *   kv_len       number of keys in the chunk (0 makes the call a no-op).
  *   m, l, o      the state, updated in place (layouts above; o 16-byte aligned).
@@ -133,6 +143,9 @@ int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
  * exact operands on the tensor cores with fp32 accumulation; the weights
  * P = e^(S - m) are rounded to fp16 once, against the running max m (the
  * largest weight of a row is exactly 1); m, l and O stay fp32 in the state.
+ * At D = 128 a CTA folds one 128-row query tile with its two softmax pipelines
+ * taking alternate 64-key tiles and merges their states at the end (the same
+ * recurrence), so results match D = 64's numerics.
  * Errors: Q8A_ERR_INVALID_ARG, Q8A_ERR_MISALIGNED, Q8A_ERR_UNSUPPORTED, Q8A_ERR_CUDA.
  */
 int attn_chunk_step(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,
@@ -237,7 +250,7 @@ int64_t q8a_static_split_scratch_floats(void);
 /*
  * attn_finalize -- out_i = O_i / l_i after the last chunk [STREAM §3]; a row
  * with l_i == 0 (it saw no key) gives 0.  out is fp16 (round to nearest even),
- * [B][n_q][H][64], 16-byte aligned; l 4-byte aligned; o 16-byte aligned.
+ * [B][n_q][H][D], 16-byte aligned; l 4-byte aligned; o 16-byte aligned.
  */
 int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int32_t heads,
                   int64_t n_q, int32_t head_dim, void *stream);

@@ -15,10 +15,11 @@ MAX_ABS = 2e-3
 REL_L2 = 1e-3
 
 
-def gpu_bytes(planes, n_tokens):
-    """uint8 [B, H, stride] device planes -> numpy [B, H, n_tokens, 68]."""
+def gpu_bytes(planes, n_tokens, head_dim=64):
+    """uint8 [B, H, stride] device planes -> numpy [B, H, n_tokens, head_dim/32*34]."""
     B, H, _ = planes.shape
-    return planes[:, :, :n_tokens * 68].reshape(B, H, n_tokens, 68).cpu().numpy()
+    rb = Q.row_bytes(head_dim)
+    return planes[:, :, :n_tokens * rb].reshape(B, H, n_tokens, rb).cpu().numpy()
 
 
 def run_gpu(q, k, v, chunk, causal=True, scale=None, q_pos0=0, order=None):
@@ -28,13 +29,13 @@ def run_gpu(q, k, v, chunk, causal=True, scale=None, q_pos0=0, order=None):
     M = k.shape[1]
     k8 = Q.q8kv_quantize(k)
     v8 = Q.q8kv_quantize(v)
-    st = Q.State(B, H, n_q, q.device)
+    st = Q.State(B, H, n_q, q.device, head_dim=D)
     starts = list(range(0, M, chunk))
     if order is not None:
         starts = [starts[i] for i in order]
     for s0 in starts:
         Q.attn_chunk_step(q, k8, v8, s0, min(chunk, M - s0), st, q_pos0=q_pos0, scale=scale,
-                          causal=causal, k_offset_bytes=s0 * 68)
+                          causal=causal, k_offset_bytes=s0 * Q.row_bytes(D))
     out = Q.attn_finalize(st)
     assert_device_clean()
     return out, k8, v8, st

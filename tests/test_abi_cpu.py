@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), f"missing export {n}"
         assert n in q8attn.SIGNATURES, f"binding lacks {n}"
-    assert lib.q8a_abi_version() == 3
+    assert lib.q8a_abi_version() == 4
 
 
 def test_plane_stride(lib):
@@ -64,6 +64,10 @@ def test_quantize_validation(lib):
     assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 64, 271, s) == Q.Q8A_ERR_INVALID_ARG   # < 4*68
     assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 64, 280, s) == Q.Q8A_ERR_MISALIGNED   # % 16
     assert lib.q8kv_quantize(A4, A16, 1, 4, 2, 64, 288, s) == Q.Q8A_ERR_MISALIGNED
+    # head_dim 128: 136-byte rows
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 128, 543, s) == Q.Q8A_ERR_INVALID_ARG  # < 4*136
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 128, 552, s) == Q.Q8A_ERR_MISALIGNED  # % 16
+    assert lib.q8kv_quantize(A16, A16, 1, 4, 2, 96, 544, s) == Q.Q8A_ERR_UNSUPPORTED
     # empty problems are no-ops that never touch the device
     assert lib.q8kv_quantize(A16, A16, 0, 4, 2, 64, 288, s) == Q.Q8A_OK
     assert lib.q8kv_quantize(P(0), P(0), 1, 0, 2, 64, 0, s) == Q.Q8A_OK
@@ -72,7 +76,8 @@ def test_quantize_validation(lib):
 def test_state_and_finalize_validation(lib):
     from chunked_prefill_attention_gb300 import q8attn as Q
     s = P(0)
-    assert lib.attn_state_init(A16, A16, A16, 1, 2, 8, 128, s) == Q.Q8A_ERR_UNSUPPORTED
+    assert lib.attn_state_init(A16, A16, A16, 1, 2, 8, 96, s) == Q.Q8A_ERR_UNSUPPORTED
+    assert lib.attn_finalize(A16, A16, A16, 1, 2, 8, 32, s) == Q.Q8A_ERR_UNSUPPORTED
     assert lib.attn_state_init(P(0), A16, A16, 1, 2, 8, 64, s) == Q.Q8A_ERR_INVALID_ARG
     assert lib.attn_state_init(A16, A16, A4, 1, 2, 8, 64, s) == Q.Q8A_ERR_MISALIGNED
     assert lib.attn_state_init(A16, A16, A16, 1, 2, -8, 64, s) == Q.Q8A_ERR_INVALID_ARG
@@ -92,6 +97,8 @@ def test_chunk_step_validation(lib):
                                    n_q, hd, scale, causal, s)
 
     assert call(hd=32) == Q.Q8A_ERR_UNSUPPORTED
+    assert call(hd=128, stride=128 * 136 - 16) == Q.Q8A_ERR_INVALID_ARG   # 136-byte rows
+    assert call(hd=128, kv_len=0, k=P(0), v=P(0)) == Q.Q8A_OK
     assert call(k=P(0)) == Q.Q8A_ERR_INVALID_ARG
     assert call(stride=8703) == Q.Q8A_ERR_INVALID_ARG
     assert call(stride=8712) == Q.Q8A_ERR_MISALIGNED
@@ -192,3 +199,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(q8attn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         q8attn.load()
+
+
+def test_head_dim_128_strides_and_unsupported_calls(lib):
+    """head_dim 128 rows are four 34-byte blocks; the split and pipelined calls
+    stay at head_dim 64."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    assert lib.q8a_plane_stride_bytes_for(100, 128) == (100 * 136 + 15) // 16 * 16
+    assert lib.q8a_plane_stride_bytes_for(100, 64) == lib.q8a_plane_stride_bytes(100)
+    assert lib.q8a_plane_stride_bytes_for(100, 96) == -1
+    assert lib.q8a_plane_stride_bytes_for(-1, 128) == -1
+    s = P(0)
+    rc = lib.attn_chunk_step_split(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64, 128,
+                                   0.125, 0, 128, A16, 1 << 20, s)
+    assert rc == Q.Q8A_ERR_UNSUPPORTED and b"head_dim" in lib.q8a_last_error()
+    rc = lib.attn_chunk_step_split_static(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64,
+                                          128, 0.125, 0, 128, s)
+    assert rc == Q.Q8A_ERR_UNSUPPORTED
