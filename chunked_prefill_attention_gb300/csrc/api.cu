@@ -256,6 +256,43 @@ int attn_chunk_step(const void* q, int64_t q_pos0, const void* k_q8, const void*
   return ok();
 }
 
+}  // extern "C"
+
+// attn_chunk_step restricted to the 128-row query tiles [tile_begin, tile_end)
+// (rows outside them are left as they are); the pipelined prefill uses it to
+// start the first chunk's step on the query rows that have arrived.
+int q8a::chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                          int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
+                          float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
+                          int32_t head_dim, float scale, int32_t causal, int64_t tile_begin,
+                          int64_t tile_end, cudaStream_t stream) {
+  const char* fn = "attn_chunk_step";
+  CUtensorMap qmap;
+  q8a::ChunkArgs a;
+  bool empty = false;
+  if (int rc = prepare_chunk_step(fn, q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start,
+                                  kv_len, m, l, o, batch, heads, n_q, head_dim, scale, causal,
+                                  &qmap, &a, &empty))
+    return rc;
+  if (empty) return ok();
+  const int64_t t0 = tile_begin > a.tile0 ? tile_begin : a.tile0;
+  const int64_t t1 = tile_end < a.tile0 + a.n_qtiles ? tile_end : a.tile0 + a.n_qtiles;
+  if (t1 <= t0) return ok();
+  // at head_dim 64 a CTA folds two consecutive tiles: a range ending inside the
+  // query rows must hold an even number of them, or its last CTA would also fold
+  // the first tile after the range
+  if (head_dim == 64 && (t1 - t0) % 2 != 0 && t1 * 128 < n_q)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: an interior range of an odd number of query tiles", fn);
+  a.tile0 = static_cast<int32_t>(t0);
+  a.n_qtiles = static_cast<int32_t>(t1 - t0);
+  cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, stream)
+                                  : q8a::launch_chunk_step(qmap, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+extern "C" {
+
 int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
                                    int64_t split_keys) {
   if (batch < 0 || heads <= 0 || n_q < 0 || kv_len < 0 || split_keys <= 0) return -1;

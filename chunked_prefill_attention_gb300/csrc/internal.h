@@ -86,6 +86,13 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
 // no split form.
 cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
 
+// attn_chunk_step for the 128-row query tiles [tile_begin, tile_end) only.
+int chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                     int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
+                     float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
+                     float scale, int32_t causal, int64_t tile_begin, int64_t tile_end,
+                     cudaStream_t stream);
+
 // Record `msg` as the calling thread's last error (q8a_last_error) and return code.
 int set_error(int code, const char* fn, const char* msg);
 

@@ -65,16 +65,16 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
   cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
   const int64_t row_floats = static_cast<int64_t>(heads) * Q8A_HEAD_DIM;   // one token, all heads
-  const size_t q_bytes = static_cast<size_t>(batch * n_tokens * row_floats) * 2;
   // slot s holds K at kv_slots + 2*s*part and V at kv_slots + (2*s+1)*part, each
   // [B][slot_tokens][H][64] (a shorter last chunk keeps the per-sequence stride)
   const int64_t part = batch * slot_tokens * row_floats;
 
   // ev: a chunk's inputs are on the device (copy stream -> compute stream);
+  // ev_q: a block of query rows is on the device (copy -> compute);
   // ev_fin: a row block of the output is final (compute stream -> copy stream);
   // ev_free[s]: slot s has been quantised and may be refilled (compute -> copy).
-  cudaEvent_t ev = nullptr, ev_fin = nullptr, ev_free[2] = {nullptr, nullptr};
-  cudaEvent_t* all[4] = {&ev, &ev_fin, &ev_free[0], &ev_free[1]};
+  cudaEvent_t ev = nullptr, ev_q = nullptr, ev_fin = nullptr, ev_free[2] = {nullptr, nullptr};
+  cudaEvent_t* all[5] = {&ev, &ev_q, &ev_fin, &ev_free[0], &ev_free[1]};
   auto release = [&]() {
     for (cudaEvent_t* p : all)   // released once the recorded work is done
       if (*p) cudaEventDestroy(*p);
@@ -109,9 +109,13 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
   // the copies below overwrite: the copy stream starts after it.
   if ((e = cudaEventRecord(ev, cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
   if ((e = cudaStreamWaitEvent(xs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
-  if ((e = cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
-    return bail(cuda_err(e, "copy of Q"));
   if ((rc = attn_state_init(m, l, o, batch, heads, n_tokens, head_dim, cs)) != Q8A_OK) return bail(rc);
+  // Q follows chunk 0's K and V on the copy stream in blocks of q_block rows
+  // (a multiple of 256, two 128-row query tiles); chunk 0's step runs block by
+  // block as the rows arrive, so only chunk 0's K and V and the first block of
+  // Q cross the link before the device starts.
+  const int64_t q_block = ((chunk < 8192 ? chunk : 8192) + 255) / 256 * 256;
+  const size_t q_row_bytes = static_cast<size_t>(row_floats) * 2;   // one token, all heads, fp16
 
   // With the causal mask (q_pos0 = 0) no later chunk touches the query rows of
   // chunk c, so they are final once its step has run: they are finalised then,
@@ -135,7 +139,7 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
           (e = cudaMemcpyAsync(vs + dst, v_host + src, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
         return bail(cuda_err(e, "copy of a K/V chunk"));
     }
-    // the chunk (and, before it on the copy stream, Q) is on the device once ev fires
+    // the chunk (and, before it on the copy stream, Q after chunk 0) is on the device once ev fires
     if ((e = cudaEventRecord(ev, xs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
     if (prev_r0 >= 0) {
       if ((e = cudaStreamWaitEvent(xs, ev_fin, 0)) != cudaSuccess ||
@@ -153,10 +157,31 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
         return bail(rc);
     }
     if ((e = cudaEventRecord(ev_free[slot], cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
-    if ((rc = attn_chunk_step(q_dev, 0, static_cast<const uint8_t*>(k8) + s0 * Q8A_ROW_BYTES,
-                              static_cast<const uint8_t*>(v8) + s0 * Q8A_ROW_BYTES, plane_stride_bytes,
-                              s0, n, m, l, o, batch, heads, n_tokens, head_dim, scale, causal, cs)) != Q8A_OK)
+    const uint8_t* kc = static_cast<const uint8_t*>(k8) + s0 * Q8A_ROW_BYTES;
+    const uint8_t* vc = static_cast<const uint8_t*>(v8) + s0 * Q8A_ROW_BYTES;
+    if (c == 0) {
+      for (int64_t r0 = 0; r0 < n_tokens; r0 += q_block) {
+        const int64_t nr = (n_tokens - r0 < q_block) ? n_tokens - r0 : q_block;
+        for (int64_t b = 0; b < batch; ++b) {
+          const size_t off = static_cast<size_t>(b * n_tokens + r0) * q_row_bytes;
+          if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(q_dev) + off,
+                                   static_cast<const uint8_t*>(q_host) + off,
+                                   static_cast<size_t>(nr) * q_row_bytes, cudaMemcpyHostToDevice, xs)) !=
+              cudaSuccess)
+            return bail(cuda_err(e, "copy of a block of Q"));
+        }
+        if ((e = cudaEventRecord(ev_q, xs)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(cs, ev_q, 0)) != cudaSuccess)
+          return bail(cuda_err(e, "cudaEventRecord / cudaStreamWaitEvent"));
+        if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
+                                        n_tokens, head_dim, scale, causal, r0 / 128, (r0 + nr + 127) / 128,
+                                        cs)) != Q8A_OK)
+          return bail(rc);
+      }
+    } else if ((rc = attn_chunk_step(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
+                                     n_tokens, head_dim, scale, causal, cs)) != Q8A_OK) {
       return bail(rc);
+    }
     if (causal) {
       if ((e = q8a::launch_finalize_rows(l, o, out_dev, batch, heads, n_tokens, head_dim, s0, n, cs)) !=
           cudaSuccess)

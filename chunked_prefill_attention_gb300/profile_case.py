@@ -19,6 +19,16 @@ warm-up launch and then --reps launches.
   ncu --set full --clock-control none -k regex:q8kv_quantize -s 1 -c 1 \\
       python -m chunked_prefill_attention_gb300.profile_case --quantize 65536
 
+With --pipelined it runs attn_prefill_pipelined on the m64k draw at --tokens
+tokens in chunks of --chunk from page-locked host buffers (one warm-up call,
+then --reps calls), so that the DRAM counters of its chunk-step launches can be
+set beside those of the device-resident step (where the whole K and V are
+quantised before the first chunk step):
+
+  ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \\
+      -k regex:chunk_step_kernel -s 8 -c 8 \\
+      python -m chunked_prefill_attention_gb300.profile_case --pipelined --tokens 65536 --reps 1
+
 With --burst CONTEXT it runs Mode B burst verification instead: the 64
 candidates of the burst_m1m draw against a CONTEXT-token, 32-head Q8_0 cache
 in key ranges of --split keys (attn_chunk_step_split, paired launches), one
@@ -44,8 +54,11 @@ def main(argv=None):
     p.add_argument("--burst", type=int, default=0)
     p.add_argument("--split", type=int, default=8192)
     p.add_argument("--quantize", type=int, default=0)
+    p.add_argument("--pipelined", action="store_true")
     a = p.parse_args(argv)
     _build.ensure_built()
+    if a.pipelined:
+        return pipelined(a)
     if a.burst > 0:
         return burst(a)
     if a.quantize > 0:
@@ -72,6 +85,31 @@ def main(argv=None):
     rows = M - (s0 // 128) * 128
     print(f"chunk {a.index} (keys {s0}..{s0 + n - 1}, query rows {s0 // 128 * 128}..{M - 1}): "
           f"{ms:.3f} ms per launch, status {rc}")
+
+
+def pipelined(a):
+    import torch
+
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
+
+    w = W.WORKLOADS["m64k"]
+    q, k, v = W.make_inputs(w, device="cuda", tokens=a.tokens)
+    B, M, H, D = q.shape
+    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    del q, k, v
+    oh = torch.empty((B, M, H, D), dtype=torch.float16).pin_memory()
+    bufs = Q.PipelineBuffers(B, M, H, torch.device("cuda"), a.chunk)
+    Q.attn_prefill_pipelined(qh, kh, vh, oh, bufs)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(a.reps):
+        Q.attn_prefill_pipelined(qh, kh, vh, oh, bufs)
+    ev[1].record()
+    torch.cuda.synchronize()
+    rc, _ = Q.device_status()
+    ms = ev[0].elapsed_time(ev[1]) / max(a.reps, 1)
+    print(f"pipelined prefill {B}x{M}x{H}x{D}, chunks of {a.chunk}: {ms:.3f} ms per call, status {rc}")
 
 
 def quantize(a):

@@ -264,7 +264,8 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  * `compute_stream` quantises and folds the chunks before it (q8kv_quantize of
  * the slot into the Q8_0 planes, attn_chunk_step with kv_start = the chunk's
  * first token, q_pos0 = 0); a slot is refilled only after the quantise that
- * read it.  The fp32 inputs so take 2 x 2 x B x chunk x H x 64 floats of device
+ * read it.  Q crosses after chunk 0's K and V, in blocks of up to 8,192 rows,
+ * and chunk 0's step runs block by block as they arrive.  The fp32 inputs so take 2 x 2 x B x chunk x H x 64 floats of device
  * memory whatever the sequence length.  With `causal` no later chunk touches a
  * chunk's own query rows, so those rows are finalised right after its step and
  * copied back to the host on copy_stream while the device works on the later
@@ -289,7 +290,7 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  *                      work already on the compute stream, so back-to-back calls
  *                      on the same buffers are ordered.  The output is on the
  *                      host once compute_stream has drained.
- * The call creates and releases four CUDA events; it allocates no memory.
+ * The call creates and releases five CUDA events; it allocates no memory.
  * Errors: Q8A_ERR_INVALID_ARG (sizes, null pointers, too small kv_slots),
  * Q8A_ERR_MISALIGNED, those of the calls above, Q8A_ERR_CUDA (a copy, event or
  * stream call failed).
