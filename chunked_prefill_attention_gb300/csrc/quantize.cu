@@ -40,21 +40,28 @@ constexpr int kThreads = 256;
 static_assert(kThreads / 32 == kHeads, "one warp per head of the block");
 constexpr int kStageBytes = 1088;   // one head's rows of a tile: 16 x 68 or 8 x 136 bytes
 
-// RN(x / d) for d > 0, from y = RN(1 / d) (see the note above).
-__device__ __forceinline__ float div_rn_by(float x, float d, float y) {
-  const float q0 = __fmul_rn(x, y);
-  const float r = __fmaf_rn(-q0, d, x);
-  return __fmaf_rn(r, y, q0);
-}
-
-// One code: round half away from zero of x / d, clamped to [-127, 127].  With
-// a finite d = 0 every code is 0; so is every code of a block whose scale
-// rounded to +inf in fp16 (amax beyond 65504 * 127), where x / inf = 0.
-__device__ __forceinline__ uint32_t code8(float x, float d, float y, bool finite_nonzero) {
-  if (!finite_nonzero) return 0u;
-  float r = roundf(div_rn_by(x, d, y));
-  r = fminf(fmaxf(r, -127.0f), 127.0f);
-  return static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu;
+// Two codes from two values, each as the low byte of a word: q = RN(x / d) by
+// the corrected quotient above (packed fp32x2), rounded half away from zero and
+// clamped to [-127, 127], every step exact in fp32:
+//   floor(RZ(a + 0.5)) is a rounded half away from zero for 0 <= a < 2^23
+//     (a + 0.5 is exact for a >= 0.5; below, round-toward-zero keeps it < 1);
+//   clamping t to 127.5 first clamps floor(t) to 127 (and catches a >= 2^23);
+//   RZ(t + 2^23) - 2^23 is floor(t) for 0.5 <= t < 2^23;
+//   RN(s + 1.5 * 2^23) holds the integer s (|s| <= 127) in its low byte, in
+//     two's complement.
+// With y = 0 and nd = 0 (scale 0, or +inf in fp16 when amax exceeds
+// 65504 * 127, where x / inf = 0) both codes are 0.
+__device__ __forceinline__ uint2 code_pair(float2 x, float2 nd2, float2 y2) {
+  const float2 q0 = __fmul2_rn(x, y2);
+  const float2 r = __ffma2_rn(q0, nd2, x);
+  const float2 qq = __ffma2_rn(r, y2, q0);
+  float2 t = __fadd2_rz(make_float2(fabsf(qq.x), fabsf(qq.y)), make_float2(0.5f, 0.5f));
+  t = make_float2(fminf(t.x, 127.5f), fminf(t.y, 127.5f));
+  const float2 m = __fadd2_rz(t, make_float2(8388608.0f, 8388608.0f));
+  const float2 f = __fadd2_rn(m, make_float2(-8388608.0f, -8388608.0f));
+  const float2 u = __fadd2_rn(make_float2(copysignf(f.x, qq.x), copysignf(f.y, qq.y)),
+                              make_float2(12582912.0f, 12582912.0f));
+  return make_uint2(__float_as_uint(u.x), __float_as_uint(u.y));
 }
 
 // 256-bit read-only load of eight consecutive floats (32-byte aligned).
@@ -122,12 +129,15 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   const float d = __half2float(d16);
   const bool finite_nonzero = d > 0.0f && d <= 65504.0f;
   const float y = finite_nonzero ? __frcp_rn(d) : 0.0f;
+  const float nd = finite_nonzero ? -d : 0.0f;
+  const float2 y2 = make_float2(y, y), nd2 = make_float2(nd, nd);
   uint32_t w[8];   // codes 4k .. 4k+3, little-endian
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    w[k] = code8(v[4 * k], d, y, finite_nonzero) | (code8(v[4 * k + 1], d, y, finite_nonzero) << 8) |
-           (code8(v[4 * k + 2], d, y, finite_nonzero) << 16) |
-           (code8(v[4 * k + 3], d, y, finite_nonzero) << 24);
+  for (int k = 0; k < 8; ++k) {
+    const uint2 c01 = code_pair(make_float2(v[4 * k], v[4 * k + 1]), nd2, y2);
+    const uint2 c23 = code_pair(make_float2(v[4 * k + 2], v[4 * k + 3]), nd2, y2);
+    w[k] = __byte_perm(__byte_perm(c01.x, c01.y, 0x0040), __byte_perm(c23.x, c23.y, 0x0040), 0x5410);
+  }
   const uint32_t dbits = __half_as_ushort(d16);
   if (valid) {
     // block bb of the row: d at 34 * bb, codes at 34 * bb + 2.  Rows start
