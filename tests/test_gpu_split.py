@@ -137,3 +137,32 @@ def test_paired_launch_continues_a_state(lib, n_q, M, chunk):
     assert_device_clean()
     want, *_ = oracle_out(q, k, v, causal=False, q_pos0=M)
     compare(out.cpu().numpy(), want, f"paired n_q{n_q} M{M} chunk{chunk}")
+
+
+def test_burst_verification_bench_shape(lib):
+    """The burst benchmark's own case: the 64 seeded candidates of the burst
+    workload against its 1,048,576-token, 32-head context, folded in key ranges
+    of 8,192 with a caller workspace, exactly as the benchmark launches it.
+    The oracle checks the Q8_0 bytes and the output of three of the heads."""
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
+    from oracle import runner as oracle_runner
+    b = W.BURSTS["burst_m1m"]
+    M, H = b.context, b.heads
+    q, k, v = W.make_burst_inputs(b, device="cuda")
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, b.queries, q.device)
+    ws = torch.empty(Q.split_workspace_floats(1, H, b.queries, M, b.split_keys), dtype=torch.float32,
+                     device="cuda")
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, st, b.split_keys, workspace=ws, q_pos0=M, causal=False)
+    out = Q.attn_finalize(st).cpu().numpy()
+    assert_device_clean()
+    heads = [0, 17, 31]
+    qn = q.cpu().numpy()
+    for h in heads:
+        wk8 = oracle_runner.quantize_kv(k[:, :, h:h + 1].contiguous().cpu().numpy())
+        assert np.array_equal(k8[:, h:h + 1, :M * 68].reshape(1, 1, M, 68).cpu().numpy(), wk8)
+        wv8 = oracle_runner.quantize_kv(v[:, :, h:h + 1].contiguous().cpu().numpy())
+        assert np.array_equal(v8[:, h:h + 1, :M * 68].reshape(1, 1, M, 68).cpu().numpy(), wv8)
+        want = oracle_runner.attention(qn[:, :, h:h + 1], wk8, wv8, 0.125, causal=False, q_pos0=M)
+        res = compare(out[:, :, h:h + 1], want, f"burst_m1m head {h}")
+        print(f"\n[burst_m1m head {h}] max|err| {res[0]:.3e} (|out| {res[2]:.2f}), rel-L2 {res[1]:.3e}")
