@@ -252,30 +252,55 @@ def time_workload(name, steps, warmup, peaks, peak_src, flush_l2, sample_clocks)
         if ev is not None:
             ev[3].record(stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    def timed(one_step, n_events):
+        for _ in range(warmup):
+            one_step()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(steps)]
+        for s in range(steps):
+            if scratch is not None:
+                scratch.zero_()
+            one_step(evs[s])
+        torch.cuda.synchronize()
+        rc, status = Q.device_status()
+        if rc != 0:
+            raise RuntimeError(f"device status {status:#x} after timing {name}")
+        return evs
+
+    tensor_bound = w.tokens >= 65536 or D == 128
     clocks = ClockSampler(dev) if sample_clocks else None
     if clocks:
         clocks.start()
-    for s in range(steps):
-        if scratch is not None:
-            scratch.zero_()
-        step(evs[s])
-    torch.cuda.synchronize()
-    clk = clocks.stop() if clocks else None
-    rc, status = Q.device_status()
-    if rc != 0:
-        raise RuntimeError(f"device status {status:#x} after timing {name}")
-    ms = sum(e[0].elapsed_time(e[3]) for e in evs) / steps
+    evs = timed(step, 4)
+    ms_calls = sum(e[0].elapsed_time(e[3]) for e in evs) / steps
     chunk_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    ms, graph_note = ms_calls, None
+    if not tensor_bound:
+        # the same step captured once into a CUDA graph (q8a_prefill_graph) and
+        # replayed with one launch: the kernels no longer wait on the host
+        g = Q.PrefillGraph(q, k, v, w.chunk)
+
+        def graph_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            g.launch(stream)
+            if ev is not None:
+                ev[1].record(stream)
+
+        gevs = timed(graph_step, 2)
+        ms = sum(e[0].elapsed_time(e[1]) for e in gevs) / steps
+        graph_note = "one q8a_prefill_graph replay per step (the same %d launches)" % (4 + len(chunks))
+        g.close()
+    clk = clocks.stop() if clocks else None
     tflops = w.causal_flops / (ms * 1e-3) / 1e12
     rec = {"workload": w.describe(), "ms_per_step": ms, "tflops": tflops,
            "tokens_per_s": B * M / (ms * 1e-3), "steps": steps, "warmup": warmup,
            "l2": ("L2 flushed before each step (256 MB write outside the timed events)" if flush_l2
                   else "inputs larger than L2")}
-    if w.tokens >= 65536 or D == 128:
+    if graph_note:
+        rec["launch"] = graph_note
+        rec["ms_per_step_launch_by_launch"] = ms_calls
+    if tensor_bound:
         peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
         achieved = w.causal_flops / (chunk_ms * 1e-3) / 1e12
         rec["roofline"] = {"bound": "tensor", "kernel": "attn_chunk_step", "achieved": achieved,
@@ -286,7 +311,7 @@ def time_workload(name, steps, warmup, peaks, peak_src, flush_l2, sample_clocks)
         hbm = float(peaks.get("hbm_gbs"))
         n_bytes = step_hbm_bytes(w)
         gbs = n_bytes / (ms * 1e-3) / 1e9
-        rec["roofline"] = {"bound": "hbm", "kernel": "whole step (%d launches)" % (4 + len(chunks)),
+        rec["roofline"] = {"bound": "hbm", "kernel": "whole step (%d kernels)" % (4 + len(chunks)),
                            "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                            "algorithmic_bytes": n_bytes, "peak_kind": f"HBM copy, {peak_src}"}
     rec["clocks"] = clk

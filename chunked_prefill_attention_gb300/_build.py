@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libq8attn.so")
-SOURCES = ["api.cu", "quantize.cu", "state.cu", "chunk_step.cu", "pipeline.cu"]
+SOURCES = ["api.cu", "quantize.cu", "state.cu", "chunk_step.cu", "pipeline.cu", "graph.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -66,7 +66,7 @@ def build(verbose=False):
 
 
 SANITIZED_LIB = os.path.join(PKG, "libq8attn_sanitized.so")
-HOST_SOURCES = ["api.cu", "pipeline.cu"]   # the C-ABI layer: validation, streams, events
+HOST_SOURCES = ["api.cu", "pipeline.cu", "graph.cu"]   # the C-ABI layer: validation, streams, events, graphs
 
 
 def build_sanitized():

@@ -66,6 +66,8 @@ int q8a::set_error(int code, const char* fn, const char* msg) {
   return fail(code, "%s: %s", fn, msg);
 }
 
+int q8a::clear_error() { return ok(); }
+
 const char* q8a::launch_note() { return g_note; }
 
 void q8a::set_launch_note(const char* fmt, ...) {

@@ -95,6 +95,8 @@ int chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const void
 
 // Record `msg` as the calling thread's last error (q8a_last_error) and return code.
 int set_error(int code, const char* fn, const char* msg);
+// Clear the calling thread's last error and return Q8A_OK (a call that succeeded).
+int clear_error();
 
 // A launcher that refuses a launch configuration describes why here (thread
 // local; "" when the last refusal had no note).

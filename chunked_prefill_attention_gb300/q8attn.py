@@ -51,6 +51,10 @@ SIGNATURES = {
     "attn_prefill_pipelined": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, _I64, _I32, _I64, _F, _I32,
                                               _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "q8a_prefill_slot_floats": (_I64, [_I64, _I32, _I64]),
+    "q8a_prefill_graph_create": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _I32,
+                                                _I64, _I32, _I64, _F, _I32, ctypes.POINTER(_P)]),
+    "q8a_prefill_graph_launch": (ctypes.c_int, [_P, _P]),
+    "q8a_prefill_graph_destroy": (ctypes.c_int, [_P]),
     "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
     "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),
     "q8a_test_inject": (ctypes.c_int, [_I32]),
@@ -238,6 +242,49 @@ def prefill_attention(q, k, v, chunk, scale=None, causal=True, k8=None, v8=None,
                         k_offset_bytes=s0 * row_bytes(D))
     out = attn_finalize(state, out)
     return out, k8, v8
+
+
+class PrefillGraph:
+    """prefill_attention captured once into a CUDA graph
+    (q8a_prefill_graph_create) and replayed with one launch per call.  The
+    graph keeps the tensors' addresses: their contents may change between
+    launches, so a new prefill of the same shape writes its Q, K and V into
+    .q/.k/.v (the caller's tensors) and launches again."""
+
+    def __init__(self, q, k, v, chunk, scale=None, causal=True):
+        B, M, H, D = q.shape
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        self.q, self.k, self.v = q, k, v
+        self.stride = plane_stride(M, D)
+        self.k8 = torch.empty((B, H, self.stride), dtype=torch.uint8, device=q.device)
+        self.v8 = torch.empty((B, H, self.stride), dtype=torch.uint8, device=q.device)
+        self.state = State(B, H, M, q.device, init=False, head_dim=D)
+        self.out = torch.empty((B, M, H, D), dtype=torch.float16, device=q.device)
+        self._h = None
+        h = ctypes.c_void_p()
+        st = self.state
+        with torch.cuda.device(q.device):
+            _check(load().q8a_prefill_graph_create(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(self.k8), _ptr(self.v8), self.stride, _ptr(st.m),
+                _ptr(st.l), _ptr(st.o), _ptr(self.out), B, H, M, D, chunk, scale, int(bool(causal)),
+                ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        """Enqueue one replay on `stream` (default: the current stream); returns .out."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.out.device)
+        with torch.cuda.device(self.out.device):
+            _check(load().q8a_prefill_graph_launch(self._h, ctypes.c_void_p(s.cuda_stream)))
+        return self.out
+
+    def close(self):
+        if self._h is not None and _lib is not None:
+            _lib.q8a_prefill_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        self.close()
 
 
 class PipelineBuffers:

@@ -56,8 +56,9 @@ extern "C" {
 /* Raised whenever an entry point is added or its contract changes.  2: the
  * split, allocation-free split, pipelined and grouped-query calls.  3: the
  * pipelined call streams K and V through two chunk slots (kv_slots).  4:
- * head_dim 128 and q8a_plane_stride_bytes_for. */
-#define Q8A_ABI_VERSION 4u
+ * head_dim 128 and q8a_plane_stride_bytes_for.  5: the captured prefill
+ * (q8a_prefill_graph_*). */
+#define Q8A_ABI_VERSION 5u
 
 enum {
   Q8A_OK = 0,
@@ -305,6 +306,52 @@ int attn_prefill_pipelined(const void *q_host, const float *k_host, const float 
 /* Floats of kv_slots attn_prefill_pipelined needs: 4 * batch * chunk * heads * 64
  * (two slots of one chunk's fp32 K and V); -1 for invalid sizes. */
 int64_t q8a_prefill_slot_floats(int64_t batch, int32_t heads, int64_t chunk);
+
+/*
+ * q8a_prefill_graph_create -- capture one whole device-resident prefill into a
+ * CUDA graph, to be replayed with q8a_prefill_graph_launch ([STREAM §3]: the
+ * chunks folded in order into the persistent state, then the final division).
+ * The graph holds, in this order, the launches of: q8kv_quantize of k into k8
+ * and of v into v8; attn_state_init of (m, l, o); attn_chunk_step for the
+ * chunks [s0, s0 + chunk) of the sequence in order (kv_start = s0, q_pos0 = 0,
+ * the chunk's slice of k8 and v8); attn_finalize of (l, o) into out.  A replay
+ * computes exactly what those calls compute when made one by one on a stream,
+ * with one host launch instead of one per kernel, so short prefills do not
+ * leave the device waiting on the host between kernels.
+ *   q, out        fp16 [B][n_tokens][H][D] device buffers, 16-byte aligned;
+ *   k, v          fp32 [B][n_tokens][H][D] device buffers, 16-byte aligned;
+ *   k8, v8        the Q8_0 planes written by the replay (layout and stride as
+ *                 for q8kv_quantize);
+ *   m, l, o       the state (layouts above);
+ *   chunk         tokens per chunk: a positive multiple of 4 at D = 64, of 2
+ *                 at D = 128;
+ *   scale, causal as for attn_chunk_step;
+ *   graph_out     receives the handle (NULL on failure).
+ * The graph keeps the pointers and sizes it was created with (and the device
+ * wait budget then in force): the caller keeps every buffer alive and in place
+ * until q8a_prefill_graph_destroy, and may change their contents between
+ * replays.  The launches are recorded on a private stream of the current
+ * device; nothing runs during the call, and no device buffer is allocated.
+ * Errors: Q8A_ERR_INVALID_ARG (null pointers, sizes, chunk, stride, scale),
+ * Q8A_ERR_UNSUPPORTED (head_dim), Q8A_ERR_MISALIGNED and the other errors of
+ * the captured calls, Q8A_ERR_CUDA (stream capture or instantiation failed).
+ */
+typedef struct q8a_prefill_graph q8a_prefill_graph;
+int q8a_prefill_graph_create(const void *q, const float *k, const float *v, void *k8, void *v8,
+                             int64_t plane_stride_bytes, float *m, float *l, float *o, void *out,
+                             int64_t batch, int32_t heads, int64_t n_tokens, int32_t head_dim,
+                             int64_t chunk, float scale, int32_t causal,
+                             q8a_prefill_graph **graph_out);
+
+/* Enqueue one replay of the captured prefill on `stream` (asynchronous).  The
+ * current device must be the one the graph was created on.  Replays on one
+ * stream run one after another.
+ * Errors: Q8A_ERR_INVALID_ARG (null handle, other device), Q8A_ERR_CUDA. */
+int q8a_prefill_graph_launch(q8a_prefill_graph *graph, void *stream);
+
+/* Release the graph (NULL is allowed).  Replays already enqueued finish first
+ * (CUDA keeps the graph's resources until they have run). */
+int q8a_prefill_graph_destroy(q8a_prefill_graph *graph);
 
 /*
  * q8a_device_status -- read (and optionally clear) the status word of the

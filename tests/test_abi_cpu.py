@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), f"missing export {n}"
         assert n in q8attn.SIGNATURES, f"binding lacks {n}"
-    assert lib.q8a_abi_version() == 4
+    assert lib.q8a_abi_version() == 5
 
 
 def test_plane_stride(lib):
@@ -183,6 +183,31 @@ def test_pipelined_prefill_validation(lib):
     assert call(slots=P(0x100008)) == Q.Q8A_ERR_MISALIGNED
     assert call(B=0) == Q.Q8A_OK
     assert call(M=0) == Q.Q8A_OK
+
+
+def test_prefill_graph_validation(lib):
+    """q8a_prefill_graph_create checks its arguments before any CUDA call and
+    leaves the handle NULL on failure; launch and destroy accept NULL safely."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    h = P(0x1234)
+
+    def create(*, ptrs=A16, stride=16 * 68, B=1, H=2, M=16, D=64, chunk=8, scale=0.125, out=True):
+        return lib.q8a_prefill_graph_create(ptrs, A16, A16, A16, A16, stride, A16, A16, A16, A16, B, H, M, D,
+                                            chunk, scale, 1, ctypes.byref(h) if out else None)
+
+    assert create(out=False) == Q.Q8A_ERR_INVALID_ARG
+    assert "graph_out" in _err(lib)
+    for kw in (dict(B=-1), dict(H=0), dict(M=-1), dict(chunk=0), dict(chunk=6), dict(ptrs=P(0)),
+               dict(stride=15 * 68), dict(stride=16 * 68 + 4), dict(scale=0.0)):
+        h.value = 0x1234
+        assert create(**kw) == Q.Q8A_ERR_INVALID_ARG, kw
+        assert not h.value, kw
+    assert create(D=32) == Q.Q8A_ERR_UNSUPPORTED
+    assert "head_dim" in _err(lib)
+    assert create(D=128, chunk=3, stride=Q.plane_stride(16, 128)) == Q.Q8A_ERR_INVALID_ARG
+    assert "chunk" in _err(lib)
+    assert lib.q8a_prefill_graph_launch(None, None) == Q.Q8A_ERR_INVALID_ARG
+    assert lib.q8a_prefill_graph_destroy(None) == Q.Q8A_OK
 
 
 def test_runtime_knobs_validation(lib):
