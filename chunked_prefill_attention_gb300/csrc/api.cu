@@ -211,6 +211,7 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
   if (cr != CUDA_SUCCESS) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", fn, (int)cr);
 
   *a = q8a::ChunkArgs{};
+  a->q = static_cast<const uint8_t*>(q);
   a->k8 = static_cast<const uint8_t*>(k_q8);
   a->v8 = static_cast<const uint8_t*>(v_q8);
   a->m = m;

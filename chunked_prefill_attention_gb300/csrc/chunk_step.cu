@@ -1446,6 +1446,500 @@ chunk_step_d128_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs
 
 }  // namespace d128
 
+// ---------------------------------------------------------------------------
+// head_dim 128, two query tiles per CTA.  The paired kernel above dequantises
+// every 64-key tile for one 128-row query tile; here the CTA's two softmax
+// pipelines take two query tiles (rows r0 .. r0+127 and r0+128 .. r0+255) and
+// both fold every key tile, so each dequantised tile serves 256 query rows, as
+// in the head_dim 64 kernel.  The room comes from keeping Q in TMEM: each
+// softmax thread stores its query row there once (column c holds channels 2c
+// and 2c+1, the layout of an A operand), QK_x reads it as A, and shared memory
+// holds only the dequantised ring and the raw ring.
+//   QK_x: M = 128, N = 64 keys, 16 MMAs of K = 16 (Q.K_hi, Q.K_lo), A in TMEM.
+//   PV_x: M = 128, N = 128 channels, 8 MMAs (P.V_hi, P.V_lo) into O_x.
+// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384),
+// Q_A [384,448), Q_B [448,512).
+// Shared memory: two dequantised stages of 64 KB (K_hi, K_lo, V_hi, V_lo of one
+// key tile, each two 8 KB atom columns of 64 keys x 128 B) and a two-stage raw
+// ring of 2 x 8,704 B.  The MMA order and the stage releases follow the head_dim
+// 64 kernel: PV_A(t), QK_A(t+1), PV_B(t), QK_B(t+1); a stage half is released
+// once both tiles' MMAs on it are issued.
+namespace d128x2 {
+
+constexpr int D = 128;
+constexpr int BM = 128;
+constexpr int NQT = 2;
+constexpr int BN = 64;
+constexpr int ROWB = 136;
+constexpr int RAWB = BN * ROWB;        // 8704
+constexpr int NR = 2;
+constexpr int ND = 2;
+constexpr int kThreads = 512;
+constexpr int kRegSoftmax = 136;
+constexpr int kRegOther = 120;
+static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split");
+
+constexpr int TILE = 16384;                       // one 64-key x 128-channel fp16 tile
+constexpr int DQ_KHI = 0, DQ_KLO = TILE, DQ_VHI = 2 * TILE, DQ_VLO = 3 * TILE;
+constexpr int DEQ_BYTES = 4 * TILE;
+constexpr int ATOMC = 8192;                       // one 64-channel atom column of a tile
+constexpr int OFF_DEQ = 0;
+constexpr int OFF_RAW = OFF_DEQ + ND * DEQ_BYTES;  // [NR][K raw | V raw]
+constexpr int OFF_BAR = OFF_RAW + NR * 2 * RAWB;
+constexpr int B_QFULL = 0;                   // NQT: Q_x is in TMEM
+constexpr int B_RAWFULL = B_QFULL + NQT;     // NR
+constexpr int B_RAWEMPTY = B_RAWFULL + NR;   // NR
+constexpr int B_KFULL = B_RAWEMPTY + NR;     // ND
+constexpr int B_KEMPTY = B_KFULL + ND;       // ND
+constexpr int B_VFULL = B_KEMPTY + ND;       // ND
+constexpr int B_VEMPTY = B_VFULL + ND;       // ND
+constexpr int B_SFULL = B_VEMPTY + ND;       // NQT
+constexpr int B_PFULL = B_SFULL + NQT;       // NQT
+constexpr int B_ODONE = B_PFULL + NQT;       // NQT
+constexpr int B_DRAIN = B_ODONE + NQT;
+constexpr int NBAR = B_DRAIN + 1;
+constexpr int OFF_CTL = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
+constexpr int SMEM_USED = OFF_CTL + CTL_BYTES;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(OFF_RAW % 16 == 0 && RAWB % 16 == 0, "bulk copy alignment");
+static_assert(OFF_DEQ % 1024 == 0 && TILE % 1024 == 0 && ATOMC % 1024 == 0, "swizzle atom alignment");
+static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+
+constexpr uint32_t T_S = 0;      // + 64 * tile
+constexpr uint32_t T_O = 128;    // + 128 * tile
+constexpr uint32_t T_Q = 384;    // + 64 * tile
+
+struct Unit {
+  int64_t bh, b, h, r0;   // (batch*heads index), first row of tile A
+  int T[NQT];             // key tiles each query tile folds (0 = inactive)
+  int T_all;              // key tiles streamed through the CTA
+};
+
+// a.n_qtiles counts 128-row query tiles from a.tile0; a CTA takes two of them,
+// and a tile past the count is inactive even when its rows exist (a launch may
+// cover a range of query tiles)
+__device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
+  Unit u;
+  const int64_t units = (static_cast<int64_t>(a.n_qtiles) + 1) / 2;
+  const int64_t idx = blockIdx.x;
+  u.bh = idx / units;
+  const int64_t qu = units - 1 - (idx % units);   // heavy units first
+  u.b = u.bh / a.heads;
+  u.h = u.bh % a.heads;
+  u.r0 = (static_cast<int64_t>(a.tile0) + 2 * qu) * BM;
+  u.T_all = 0;
+#pragma unroll
+  for (int x = 0; x < NQT; ++x) {
+    const int64_t rx = u.r0 + x * BM;
+    u.T[x] = 0;
+    if (2 * qu + x < a.n_qtiles && rx < a.n_q) {
+      const int64_t r_last = i64min(rx + BM - 1, a.n_q - 1);
+      int64_t n_vis = a.kv_len;
+      if (a.causal) n_vis = i64min(n_vis, a.q_pos0 + r_last - a.kv_start + 1);
+      u.T[x] = n_vis > 0 ? static_cast<int>((n_vis + BN - 1) / BN) : 0;
+    }
+    u.T_all = max(u.T_all, u.T[x]);
+  }
+  return u;
+}
+
+__device__ __forceinline__ void producer(const ChunkArgs& a, const Unit& u, uint8_t* smem, uint32_t sbase,
+                                         Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  int last_bulk[NR];
+#pragma unroll
+  for (int s = 0; s < NR; ++s) last_bulk[s] = -1;
+  const int64_t kv_plane = u.b * a.kv_heads + u.h / (a.heads / a.kv_heads);
+  const uint8_t* kp = a.k8 + kv_plane * a.plane_stride;
+  const uint8_t* vp = a.v8 + kv_plane * a.plane_stride;
+  for (int t = 0; t < u.T_all; ++t) {
+    const int sr = t % NR;
+    if (!wait_bar(bar(B_RAWEMPTY + sr), ((t / NR) & 1) ^ 1, ctl, budget, R_PRODUCER, true)) break;
+    const int64_t k0 = static_cast<int64_t>(t) * BN;
+    const int n = static_cast<int>(i64min(BN, a.kv_len - k0));
+    const uint32_t bytes = static_cast<uint32_t>(n) * ROWB;
+    const uint32_t dk = sbase + OFF_RAW + sr * 2 * RAWB;
+    if ((bytes & 15u) == 0u) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_RAWFULL + sr), 2u * bytes);
+        bulk_load(dk, kp + k0 * ROWB, bytes, bar(B_RAWFULL + sr));
+        bulk_load(dk + RAWB, vp + k0 * ROWB, bytes, bar(B_RAWFULL + sr));
+      }
+#pragma unroll
+      for (int s = 0; s < NR; ++s)
+        if (s == sr) last_bulk[s] = t;
+    } else {
+      // ragged tail whose byte count is not a multiple of 16: plain 4-byte copies
+      const uint32_t* sk = reinterpret_cast<const uint32_t*>(kp + k0 * ROWB);
+      const uint32_t* sv = reinterpret_cast<const uint32_t*>(vp + k0 * ROWB);
+      uint32_t* wk = reinterpret_cast<uint32_t*>(smem + OFF_RAW + sr * 2 * RAWB);
+      uint32_t* wv = wk + RAWB / 4;
+      const int words = n * (ROWB / 4);
+      for (int w = lane; w < words; w += 32) {
+        wk[w] = __ldg(sk + w);
+        wv[w] = __ldg(sv + w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_RAWFULL + sr));
+#pragma unroll
+      for (int s = 0; s < NR; ++s)
+        if (s == sr) last_bulk[s] = -1;
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < NR; ++s)
+    if (last_bulk[s] >= 0) wait_bar(bar(B_RAWFULL + s), (last_bulk[s] / NR) & 1, ctl, budget, R_DRAIN, false);
+}
+
+// Thread k < 64: K row k of each key tile; thread 64 + k: V row k.
+__device__ __forceinline__ void dequant(const ChunkArgs& a, const Unit& u, uint8_t* smem, uint32_t sbase,
+                                        Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  const int tid = threadIdx.x - 256;
+  const int tensor = tid >> 6;        // 0: K, 1: V
+  const int k = tid & 63;             // key row of the tile
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  const int sw = k & 7;
+  for (int t = 0; t < u.T_all; ++t) {
+    const int sr = t % NR;
+    const int sd = t % ND;
+    const uint32_t fill = static_cast<uint32_t>((t / ND) & 1);
+    if (!wait_bar(bar(B_RAWFULL + sr), (t / NR) & 1, ctl, budget, R_DEQUANT, true)) break;
+    if (!wait_bar(bar((tensor ? B_VEMPTY : B_KEMPTY) + sd), fill ^ 1, ctl, budget, R_DEQUANT, true)) break;
+    const int n_valid = static_cast<int>(i64min(BN, a.kv_len - static_cast<int64_t>(t) * BN));
+    uint8_t* hi = smem + OFF_DEQ + sd * DEQ_BYTES + (tensor ? DQ_VHI : DQ_KHI) + k * 128;
+    uint8_t* lo = smem + OFF_DEQ + sd * DEQ_BYTES + (tensor ? DQ_VLO : DQ_KLO) + k * 128;
+    if (k < n_valid) {
+      const uint32_t* raw = reinterpret_cast<const uint32_t*>(
+          smem + OFF_RAW + sr * 2 * RAWB + tensor * RAWB + k * ROWB);
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        // 9-word window: even blocks start word-aligned (scale in the low half of
+        // word 0), odd blocks 2 bytes into a word (scale in its high half)
+        const int w0 = 17 * (blk >> 1) + 8 * (blk & 1);
+        uint32_t w[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = raw[w0 + i];
+        dequant_block(w, blk & 1, hi + (blk >> 1) * ATOMC, lo + (blk >> 1) * ATOMC, sw);
+      }
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          *reinterpret_cast<uint4*>(hi + c * ATOMC + 16 * j) = z;
+          *reinterpret_cast<uint4*>(lo + c * ATOMC + 16 * j) = z;
+        }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar((tensor ? B_VFULL : B_KFULL) + sd));
+    mbar_arrive(bar(B_RAWEMPTY + sr));
+  }
+}
+
+__device__ __forceinline__ void mma(const ChunkArgs& a, const Unit& u, uint32_t sbase, uint32_t tmem,
+                                    Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  constexpr uint32_t kIdescQK = idesc_f16_f32(128, BN, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, 0, 1);
+  const bool leader = elect_one();
+  // K tiles K-major in two 64-channel atom columns 8 KB apart (k-step kk covers
+  // channels 16kk .. 16kk+15); Q_x in TMEM, 8 columns per k-step.  V tiles
+  // MN-major: the two 64-channel halves of N are 8 KB apart (leading byte
+  // offset), each k-step covers 16 keys = two 8-row swizzle atoms (2 KB).  P of
+  // keys 16kk .. 16kk+15 sits in TMEM columns 8kk .. 8kk+7 of S_x.
+  const uint64_t kdesc0 = smem_desc(sbase + OFF_DEQ + DQ_KHI, 1024, 1024, kSwizzle128);
+  const uint64_t vdesc0 = smem_desc(sbase + OFF_DEQ + DQ_VHI, ATOMC, 1024, kSwizzle128);
+  auto issue_qk = [&](int x, int sd) {
+    const uint32_t d = tmem + T_S + 64u * x;
+    const uint32_t qa = tmem + T_Q + 64u * x;
+    const uint64_t kd = kdesc0 + static_cast<uint64_t>(sd * (DEQ_BYTES >> 4));
+    if (leader) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t kb = kd + static_cast<uint64_t>((part * TILE + (kk >> 2) * ATOMC + (kk & 3) * 32) >> 4);
+          mma_ts(d, qa + 8u * kk, kb, kIdescQK, (part | kk) != 0 ? 1u : 0u);
+        }
+    }
+  };
+  auto issue_pv = [&](int x, int sd) {
+    const uint32_t o = tmem + T_O + 128u * x;
+    const uint32_t p = tmem + T_S + 64u * x;
+    const uint64_t vd = vdesc0 + static_cast<uint64_t>(sd * (DEQ_BYTES >> 4));
+    if (leader) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(o, p + 8u * kk, vd + static_cast<uint64_t>((part * TILE + kk * 2048) >> 4), kIdescPV, 1u);
+    }
+  };
+  auto commit = [&](int b) {
+    if (leader) mma_commit(bar(b));
+  };
+  // Key tile j sits in stage j % ND, filled for the (j / ND)-th time; both
+  // query tiles read it, so a stage half is released after tile B's MMA on it.
+  bool ok = true;
+#pragma unroll
+  for (int x = 0; x < NQT; ++x)
+    if (ok && u.T[x] > 0) {
+      ok = wait_bar(bar(B_QFULL + x), 0, ctl, budget, R_MMA, true) &&
+           wait_bar(bar(B_KFULL + 0), 0, ctl, budget, R_MMA, true);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk(x, 0);
+      commit(B_SFULL + x);
+    }
+  if (ok) commit(B_KEMPTY + 0);   // every reader of K(0) issued
+  for (int j = 0; ok && j < u.T_all; ++j) {
+#pragma unroll
+    for (int x = 0; x < NQT; ++x) {
+      if (j < u.T[x]) {
+        const int sd = j % ND;
+        if (!wait_bar(bar(B_VFULL + sd), static_cast<uint32_t>((j / ND) & 1), ctl, budget, R_MMA, true) ||
+            !wait_bar(bar(B_PFULL + x), static_cast<uint32_t>(j & 1), ctl, budget, R_MMA, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(x, sd);
+        if (j == u.T[x] - 1) commit(B_ODONE + x);
+      }
+      if (x == NQT - 1) commit(B_VEMPTY + j % ND);   // every reader of V(j) issued
+      if (j + 1 < u.T[x]) {
+        const int sd = (j + 1) % ND;
+        if (!wait_bar(bar(B_KFULL + sd), static_cast<uint32_t>(((j + 1) / ND) & 1), ctl, budget, R_MMA, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_qk(x, sd);
+        commit(B_SFULL + x);
+      }
+      if (x == NQT - 1 && j + 1 < u.T_all) commit(B_KEMPTY + (j + 1) % ND);
+    }
+  }
+  // never leave with an MMA in flight
+  commit(B_DRAIN);
+  __syncwarp();
+  wait_bar(bar(B_DRAIN), 0, ctl, budget, R_DRAIN, false);
+}
+
+__device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x, uint32_t sbase,
+                                        uint32_t tmem, Ctl* ctl) {
+  const uint64_t budget = 2 * a.timeout_ns;
+  const int row = threadIdx.x & 127;
+  const int wq = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  const int T = u.T[x];
+  if (T == 0) return;
+  const int64_t rg = u.r0 + static_cast<int64_t>(x) * BM + row;
+  const int64_t pos = a.q_pos0 + rg;
+  const bool active = rg < a.n_q && (!a.causal || pos >= a.kv_start);
+  const int64_t sidx = u.bh * a.n_q + rg;
+  const uint32_t t_s = tmem + lane_off + T_S + 64u * x;
+  const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
+  const uint32_t t_q = tmem + lane_off + T_Q + 64u * x;
+  {
+    // this row of Q into TMEM, the A operand of QK_x: column c holds channels
+    // 2c (low half) and 2c + 1; rows past n_q are zero
+    uint32_t qv[64];
+    if (rg < a.n_q) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((u.b * a.n_q + rg) * a.heads + u.h) * static_cast<int64_t>(D * 2));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 w = src[i];
+        qv[4 * i + 0] = w.x;
+        qv[4 * i + 1] = w.y;
+        qv[4 * i + 2] = w.z;
+        qv[4 * i + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) qv[i] = 0u;
+    }
+    tmem_st32_at<0>(t_q, qv);
+    tmem_st32_at<32>(t_q + 32, qv);
+  }
+  float m_run = -INFINITY, l_run = 0.0f;
+  if (active) {
+    m_run = a.m[sidx];
+    l_run = a.l[sidx];
+  }
+  {
+    uint32_t oh[64];
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      if (active) {
+        const float4* src = reinterpret_cast<const float4*>(a.o + sidx * D + 64 * hh);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 p = src[i];
+          oh[4 * i + 0] = __float_as_uint(p.x);
+          oh[4 * i + 1] = __float_as_uint(p.y);
+          oh[4 * i + 2] = __float_as_uint(p.z);
+          oh[4 * i + 3] = __float_as_uint(p.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) oh[i] = 0u;
+      }
+      tmem_st32_at<0>(t_o + 64 * hh, oh);
+      tmem_st32_at<32>(t_o + 64 * hh + 32, oh);
+    }
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  // test hook: the first CTA's tile A never announces its Q, so the waits on it run out
+  if (!(a.inject == 1 && blockIdx.x == 0 && x == 0)) mbar_arrive(bar(B_QFULL + x));
+
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int64_t q_first = a.q_pos0 + u.r0 + static_cast<int64_t>(x) * BM;
+  bool ok = true;
+#pragma unroll 1
+  for (int t = 0; t < T; ++t) {
+    if (!wait_bar(bar(B_SFULL + x), t & 1, ctl, budget, R_SOFTMAX, true)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t s[64];
+    d128::ld32_at<0>(t_s, s);
+    d128::ld32_at<32>(t_s + 32, s);
+    d128::wait_ld_at<0>(s);
+    d128::wait_ld_at<32>(s);
+    const int64_t k0 = static_cast<int64_t>(t) * BN;
+    const bool need_mask = (k0 + BN > a.kv_len) || (a.causal && a.kv_start + k0 + BN - 1 > q_first);
+    if (__builtin_expect(need_mask, 0)) {
+      int64_t lim = a.kv_len - 1 - k0;
+      if (a.causal) lim = i64min(lim, pos - a.kv_start - k0);
+      const int li = static_cast<int>(i64max(-1, i64min(lim, BN - 1)));
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (j > li) s[j] = __float_as_uint(-INFINITY);
+    }
+    float pm[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pm[i] = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < 32; ++p)
+      pm[p & 3] = max3(pm[p & 3], __uint_as_float(s[2 * p]), __uint_as_float(s[2 * p + 1]));
+    const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+    const float t_nat = mx * a.scale;   // -inf when every key of the tile is masked
+    float alpha = 1.0f;
+    const bool resc = t_nat > m_run;
+    if (resc) {
+      alpha = (m_run == -INFINITY) ? 0.0f : ex2_approx((m_run - t_nat) * kLog2e);
+      m_run = t_nat;
+    }
+    const float mlog = (m_run == -INFINITY) ? 0.0f : m_run * kLog2e;
+    const float2 nm2 = make_float2(-mlog, -mlog);
+    float2 rs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.0f, 0.0f);
+    uint32_t p[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float2 sv = make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+      const float2 e = __ffma2_rn(sv, sl2, nm2);
+      const float2 bt = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+      rs[i & 3] = __fadd2_rn(rs[i & 3], bt);
+      p[i] = pack_half2(bt.x, bt.y);
+    }
+    tmem_st32(t_s, p);
+    // PV_x(t-1) has completed (QK_x(t), issued after it, has): O is stable
+    if (__any_sync(0xFFFFFFFFu, resc)) d128::scale_o(t_o, alpha);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar(B_PFULL + x));
+    const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+    l_run = fmaf(l_run, alpha, r.x + r.y);
+  }
+  if (!ok) return;
+  if (!wait_bar(bar(B_ODONE + x), 0, ctl, budget, R_SOFTMAX, true)) return;
+  tc_fence_after();
+  if (active) {
+    a.m[sidx] = m_run;
+    a.l[sidx] = l_run;
+  }
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {   // 32 channels at a time
+    uint32_t ov[32];
+    tmem_ld32(t_o + 32 * q, ov);
+    tmem_wait_ld(ov);
+    if (active) {
+      float4* dst = reinterpret_cast<float4*>(a.o + sidx * D + 32 * q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                             __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chunk_step_d128x2_kernel(const ChunkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + OFF_CTL);
+  const int warp = threadIdx.x >> 5;
+  const int wg = warp >> 2;
+  const Unit u = make_unit(a);
+  if (u.T_all == 0) return;   // uniform over the CTA: no visible key for these rows
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBAR; ++i) {
+      uint32_t count = 1;
+      if (i >= B_QFULL && i < B_QFULL + NQT) count = 128;        // softmax threads of a tile
+      if (i >= B_RAWEMPTY && i < B_RAWEMPTY + NR) count = 128;   // every dequant thread
+      if (i >= B_KFULL && i < B_KFULL + ND) count = 64;          // the K threads
+      if (i >= B_VFULL && i < B_VFULL + ND) count = 64;          // the V threads
+      if (i >= B_PFULL && i < B_PFULL + NQT) count = 128;        // softmax threads of a tile
+      mbar_init(sbase + OFF_BAR + 8u * i, count);
+    }
+    ctl->abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(sbase + OFF_CTL, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  if (wg < 2) {
+    reg_alloc<kRegSoftmax>();
+    softmax(a, u, wg, sbase, tmem, ctl);
+  } else {
+    reg_dealloc<kRegOther>();
+    if (wg == 2) {
+      dequant(a, u, smem, sbase, ctl);
+    } else if (warp == 12) {
+      producer(a, u, smem, sbase, ctl);
+    } else if (warp == 13) {
+      mma(a, u, sbase, tmem, ctl);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace d128x2
+
 }  // namespace
 
 cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream) {
@@ -1506,7 +2000,36 @@ cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& arg
     }
     configured_device = dev;
   }
-  const int64_t blocks = static_cast<int64_t>(args.n_qtiles) * args.bh;   // one 128-row tile each
+  if (args.n_qtiles >= 2) {
+    // two query tiles per CTA, Q in TMEM
+    static thread_local int configured_x2 = -1;
+    if (configured_x2 != dev) {
+      e = cudaFuncSetAttribute(d128x2::chunk_step_d128x2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               d128x2::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, d128x2::chunk_step_d128x2_kernel);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs * d128x2::kThreads != 65536 || fa.maxThreadsPerBlock < d128x2::kThreads) {
+        set_launch_note("chunk_step_d128x2_kernel has %d registers per thread and at most %d threads "
+                        "per block; the register split needs %d and %d",
+                        fa.numRegs, fa.maxThreadsPerBlock, 65536 / d128x2::kThreads, d128x2::kThreads);
+        return cudaErrorInvalidConfiguration;
+      }
+      configured_x2 = dev;
+    }
+    const int64_t blocks = (static_cast<int64_t>(args.n_qtiles) + 1) / 2 * args.bh;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    d128x2::chunk_step_d128x2_kernel<<<static_cast<unsigned>(blocks), d128x2::kThreads, d128x2::SMEM_BYTES,
+                                       stream>>>(args);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+      set_launch_note("chunk_step_d128x2_kernel<<<%lld, %d, %d>>>", static_cast<long long>(blocks),
+                      d128x2::kThreads, d128x2::SMEM_BYTES);
+    return e;
+  }
+  // a single query tile: both pipelines on its rows (paired)
+  const int64_t blocks = static_cast<int64_t>(args.n_qtiles) * args.bh;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   d128::chunk_step_d128_kernel<<<static_cast<unsigned>(blocks), d128::kThreads, d128::SMEM_BYTES, stream>>>(

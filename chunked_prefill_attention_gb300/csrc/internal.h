@@ -43,6 +43,7 @@ cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int6
 
 // Arguments of one chunk-step launch (everything but the Q tensor map).
 struct ChunkArgs {
+  const uint8_t* q;       // Q fp16 [B][n_q][H][D] (the head_dim 128 kernel reads rows directly)
   const uint8_t* k8;      // chunk key 0 of plane (0,0)
   const uint8_t* v8;
   float* m;

@@ -29,6 +29,13 @@ quantised before the first chunk step):
       -k regex:chunk_step_kernel -s 8 -c 8 \\
       python -m chunked_prefill_attention_gb300.profile_case --pipelined --tokens 65536 --reps 1
 
+With --head-dim 128 the chunk-step case takes the m16k_d128 draw (seed 6, 32
+heads x 128) instead; --tokens 16384 --chunk 4096 --index 1 profiles a launch
+of keys 4,096..8,191 against query rows 4,096..16,383 (0.7 GB on the device):
+
+  ncu --set full --clock-control none -k regex:chunk_step_d128 -s 4 -c 1 \\
+      python -m chunked_prefill_attention_gb300.profile_case --head-dim 128 --chunk 4096
+
 With --burst CONTEXT it runs Mode B burst verification instead: the 64
 candidates of the burst_m1m draw against a CONTEXT-token, 32-head Q8_0 cache
 in key ranges of --split keys (attn_chunk_step_split, paired launches), one
@@ -55,6 +62,7 @@ def main(argv=None):
     p.add_argument("--split", type=int, default=8192)
     p.add_argument("--quantize", type=int, default=0)
     p.add_argument("--pipelined", action="store_true")
+    p.add_argument("--head-dim", type=int, default=64, choices=(64, 128))
     a = p.parse_args(argv)
     _build.ensure_built()
     if a.pipelined:
@@ -63,21 +71,22 @@ def main(argv=None):
         return burst(a)
     if a.quantize > 0:
         return quantize(a)
-    w = W.WORKLOADS["m64k"]
+    w = W.WORKLOADS["m64k" if a.head_dim == 64 else "m16k_d128"]
     q, k, v = W.make_inputs(w, device="cuda", tokens=a.tokens)
-    B, M, H, _ = q.shape
+    B, M, H, D = q.shape
+    rb = Q.row_bytes(D)
     k8 = Q.q8kv_quantize(k)
     v8 = Q.q8kv_quantize(v)
-    st = Q.State(B, H, M, q.device)
+    st = Q.State(B, H, M, q.device, head_dim=D)
     starts = list(range(0, M, a.chunk))
     for s0 in starts:
-        Q.attn_chunk_step(q, k8, v8, s0, min(a.chunk, M - s0), st, k_offset_bytes=s0 * 68)
+        Q.attn_chunk_step(q, k8, v8, s0, min(a.chunk, M - s0), st, k_offset_bytes=s0 * rb)
     s0 = starts[a.index]
     n = min(a.chunk, M - s0)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     ev[0].record()
     for _ in range(a.reps):
-        Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * 68)
+        Q.attn_chunk_step(q, k8, v8, s0, n, st, k_offset_bytes=s0 * rb)
     ev[1].record()
     torch.cuda.synchronize()
     rc, status = Q.device_status()
