@@ -53,14 +53,26 @@ finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4
     const float lv = __ldg(l + row);
     const float4 a = __ldg(o + row * (kD / 4) + 2 * part);
     const float4 c = __ldg(o + row * (kD / 4) + 2 * part + 1);
-    float y[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    // o / l rounded to fp32 without a divide per value: with r = RN(1 / l),
+    // q0 = RN(o r) and the exact residual o - q0 l (one fma), RN(q0 + res r) is
+    // the correctly rounded quotient (Markstein's correction) for every normal
+    // quotient; a subnormal one rounds to an fp16 zero either way.
+    const bool seen = lv > 0.0f;
+    const float rc = seen ? __frcp_rn(lv) : 0.0f;
+    const float2 r2 = make_float2(rc, rc);
+    const float2 nl2 = make_float2(-lv, -lv);
+    float2 y[4] = {make_float2(a.x, a.y), make_float2(a.z, a.w), make_float2(c.x, c.y), make_float2(c.z, c.w)};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = (lv > 0.0f) ? __fdiv_rn(y[i], lv) : 0.0f;
+    for (int i = 0; i < 4; ++i) {
+      const float2 q0 = __fmul2_rn(y[i], r2);
+      const float2 res = __ffma2_rn(q0, nl2, y[i]);
+      y[i] = seen ? __ffma2_rn(res, r2, q0) : make_float2(0.0f, 0.0f);
+    }
     uint4 pk;
-    __half2 h0 = __floats2half2_rn(y[0], y[1]);
-    __half2 h1 = __floats2half2_rn(y[2], y[3]);
-    __half2 h2 = __floats2half2_rn(y[4], y[5]);
-    __half2 h3 = __floats2half2_rn(y[6], y[7]);
+    __half2 h0 = __floats2half2_rn(y[0].x, y[0].y);
+    __half2 h1 = __floats2half2_rn(y[1].x, y[1].y);
+    __half2 h2 = __floats2half2_rn(y[2].x, y[2].y);
+    __half2 h3 = __floats2half2_rn(y[3].x, y[3].y);
     pk.x = *reinterpret_cast<uint32_t*>(&h0);
     pk.y = *reinterpret_cast<uint32_t*>(&h1);
     pk.z = *reinterpret_cast<uint32_t*>(&h2);

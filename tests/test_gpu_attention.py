@@ -144,6 +144,26 @@ def test_state_init_and_finalize_values(lib):
     assert torch.equal(out[1, 5, 2].float(), (torch.arange(64, device="cuda") / 4.0).half().float())
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_finalize_is_the_rounded_quotient(lib, D):
+    """attn_finalize gives fp16(RN_fp32(O / l)): the fp32 quotient it forms
+    without a divide per value equals the IEEE quotient (torch's division),
+    bit for bit, over a wide spread of O and l; rows with l == 0 give 0."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    g = torch.Generator(device="cuda")
+    g.manual_seed(D)
+    st = Q.State(2, 5, 300, "cuda", head_dim=D)
+    st.l.copy_(torch.exp(torch.rand(st.l.shape, generator=g, device="cuda") * 20.0 - 2.0))
+    st.l[0, 1, :7] = 0.0
+    st.o.copy_(torch.randn(st.o.shape, generator=g, device="cuda") * st.l[..., None] *
+               torch.rand(st.o.shape, generator=g, device="cuda") * 8.0)
+    out = Q.attn_finalize(st)
+    want = torch.where(st.l[..., None] > 0, st.o / st.l[..., None], torch.zeros_like(st.o))
+    want = want.permute(0, 2, 1, 3).half()
+    assert torch.equal(out, want)
+    assert torch.all(out[0, :7, 1] == 0)
+
+
 def test_rows_before_chunk_keep_state(lib):
     """A causal chunk starting at key 256 leaves the state of rows 0..255 untouched."""
     from chunked_prefill_attention_gb300 import q8attn as Q
