@@ -56,8 +56,10 @@ def test_d128_quantize_input_only_16_byte_aligned(lib):
 def test_d128_causal_parity_small(lib, B, M, H, chunk):
     """Chunk starts are even (a 136-byte row offset is 16-byte aligned only
     then); a ragged last tile of odd length has a byte count that is not a
-    multiple of 16 (copied with plain loads); rows of a query tile fold both
-    pipelines' key tiles and merge them."""
+    multiple of 16 (copied with plain loads).  Launches over one query tile run
+    the paired kernel (both pipelines on its rows, merged at the end); launches
+    over two or more run the two-query-tile kernel, including odd tile counts
+    (300, 333 and 1030 tokens) and chunks whose first visible tile is not 0."""
     q, k, v = _inputs(B, M, H, seed=M * 5 + B)
     out, k8, v8, _ = run_gpu(q, k, v, chunk)
     want, wk8, wv8 = oracle_out(q, k, v)

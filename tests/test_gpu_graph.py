@@ -96,3 +96,26 @@ def test_graph_without_mask_and_on_another_stream(lib):
     want, *_ = oracle_out(q, k, v, causal=False)
     compare(g.out.cpu().numpy(), want, "graph, no mask")
     g.close()
+
+
+def test_graph_create_reports_a_failing_call_and_leaves_no_capture(lib):
+    """A captured call that rejects its arguments (here a K buffer that is only
+    4-byte aligned) makes the create fail with that call's code and no handle;
+    the capture is ended, so a following create and replay work."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    from tests.parity import seeded
+    B, M, H = 1, 256, 2
+    q = seeded((B, M, H, 64), 91, "cuda", torch.float16)
+    k_buf = seeded((B * M * H * 64 + 4,), 92, "cuda")
+    v = seeded((B, M, H, 64), 93, "cuda")
+    k_bad = k_buf[1:1 + B * M * H * 64].view(B, M, H, 64)
+    with pytest.raises(Q.Q8AttnError) as err:
+        Q.PrefillGraph(q, k_bad, v, 128)
+    assert err.value.code == Q.Q8A_ERR_MISALIGNED
+    k = k_bad.clone()
+    g = Q.PrefillGraph(q, k, v, 128)
+    g.launch()
+    torch.cuda.synchronize()
+    assert_device_clean()
+    _same(g, _eager(q, k, v, 128), M, 64)
+    g.close()
