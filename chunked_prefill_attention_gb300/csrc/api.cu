@@ -68,6 +68,13 @@ int q8a::set_error(int code, const char* fn, const char* msg) {
 
 int q8a::clear_error() { return ok(); }
 
+namespace {
+thread_local bool g_pdl = false;
+}  // namespace
+bool q8a::pdl_enabled() { return g_pdl; }
+q8a::PdlScope::PdlScope() : prev(g_pdl) { g_pdl = true; }
+q8a::PdlScope::~PdlScope() { g_pdl = prev; }
+
 const char* q8a::launch_note() { return g_note; }
 
 void q8a::set_launch_note(const char* fmt, ...) {

@@ -846,6 +846,8 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();
+  pdl_wait();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -1394,6 +1396,8 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_step_d128_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();
+  pdl_wait();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -1888,6 +1892,8 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_step_d128x2_kernel(const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();
+  pdl_wait();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -1972,8 +1978,8 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const unsigned gy = args.split_keys > 0 ? static_cast<unsigned>(args.n_splits) : 1u;
-  chunk_step_kernel<<<dim3(static_cast<unsigned>(blocks), gy), kThreads, SMEM_BYTES, stream>>>(qmap, units);
-  e = cudaGetLastError();
+  e = launch_kernel(chunk_step_kernel, dim3(static_cast<unsigned>(blocks), gy), dim3(kThreads), SMEM_BYTES, stream,
+                    qmap, units);
   if (e != cudaSuccess)
     set_launch_note("chunk_step_kernel<<<(%lld, %u), %d, %d>>>", static_cast<long long>(blocks), gy,
                     kThreads, SMEM_BYTES);
@@ -2020,9 +2026,8 @@ cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& arg
     }
     const int64_t blocks = (static_cast<int64_t>(args.n_qtiles) + 1) / 2 * args.bh;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    d128x2::chunk_step_d128x2_kernel<<<static_cast<unsigned>(blocks), d128x2::kThreads, d128x2::SMEM_BYTES,
-                                       stream>>>(args);
-    e = cudaGetLastError();
+    e = launch_kernel(d128x2::chunk_step_d128x2_kernel, dim3(static_cast<unsigned>(blocks)), dim3(d128x2::kThreads),
+                      d128x2::SMEM_BYTES, stream, args);
     if (e != cudaSuccess)
       set_launch_note("chunk_step_d128x2_kernel<<<%lld, %d, %d>>>", static_cast<long long>(blocks),
                       d128x2::kThreads, d128x2::SMEM_BYTES);
@@ -2032,9 +2037,8 @@ cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& arg
   const int64_t blocks = static_cast<int64_t>(args.n_qtiles) * args.bh;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  d128::chunk_step_d128_kernel<<<static_cast<unsigned>(blocks), d128::kThreads, d128::SMEM_BYTES, stream>>>(
-      qmap, args);
-  e = cudaGetLastError();
+  e = launch_kernel(d128::chunk_step_d128_kernel, dim3(static_cast<unsigned>(blocks)), dim3(d128::kThreads),
+                    d128::SMEM_BYTES, stream, qmap, args);
   if (e != cudaSuccess)
     set_launch_note("chunk_step_d128_kernel<<<%lld, %d, %d>>>", static_cast<long long>(blocks),
                     d128::kThreads, d128::SMEM_BYTES);

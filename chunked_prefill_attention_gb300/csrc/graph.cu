@@ -92,8 +92,15 @@ int q8a_prefill_graph_create(const void* q, const float* k, const float* v, void
     cudaStreamDestroy(cs);
     return cuda_err(e, kCreate, "cudaStreamBeginCapture");
   }
-  const int rc = enqueue_prefill(q, k, v, k8, v8, plane_stride_bytes, m, l, o, out, batch, heads, n_tokens,
-                                 head_dim, chunk, scale, causal, cs);
+  int rc;
+  {
+    // consecutive kernels of the graph with programmatic dependencies: each
+    // may be scheduled while its predecessor's last CTAs run, and waits for
+    // the predecessor's completion before it touches memory
+    q8a::PdlScope pdl;
+    rc = enqueue_prefill(q, k, v, k8, v8, plane_stride_bytes, m, l, o, out, batch, heads, n_tokens, head_dim,
+                         chunk, scale, causal, cs);
+  }
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
   cudaStreamDestroy(cs);

@@ -20,6 +20,38 @@ struct NvtxRange {
 };
 
 
+// Programmatic dependent launch of the library's kernels: while a PdlScope is
+// alive on the calling thread (the captured prefill sets one during stream
+// capture), every kernel is launched with programmatic stream serialization,
+// so the device may schedule it while its predecessor's last CTAs run; each
+// kernel waits for the predecessor's completion before touching memory.
+bool pdl_enabled();
+struct PdlScope {
+  PdlScope();
+  ~PdlScope();
+  PdlScope(const PdlScope&) = delete;
+  PdlScope& operator=(const PdlScope&) = delete;
+  bool prev;
+};
+
+// kernel<<<grid, block, smem, stream>>>(args...), with programmatic stream
+// serialization when pdl_enabled().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kHeadDim = 64;
 constexpr int kRowBytes = 68;  // one head row: two 34-byte Q8_0 blocks
 

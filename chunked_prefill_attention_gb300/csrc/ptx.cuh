@@ -124,6 +124,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream be scheduled once every CTA of this one has started (or exited);
+// wait blocks until the kernel this one depends on has completed and its
+// writes are visible.  Every kernel of the library calls both first, before
+// any global memory access, so a programmatic launch can never expose a
+// predecessor's partial results; without a programmatic dependency both
+// return at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16, one CTA.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {

@@ -86,6 +86,8 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   constexpr int kTok = 32 / kBlk;
   static_assert(kTok * kRow == kStageBytes, "staging rows of one head");
   __shared__ __align__(16) uint8_t stage[kHeads][kStageBytes];
+  pdl_launch_dependents();
+  pdl_wait();
 
   const int64_t blk = blockIdx.x;
   const int ht = static_cast<int>(blk % head_tiles);
@@ -184,10 +186,8 @@ cudaError_t launch_quantize_d(const float* x, uint8_t* out, int64_t batch, int64
   if (blocks > 0x7FFFFFFF || tok_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const bool wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0;
   auto kernel = wide ? q8kv_quantize_kernel<kD, true> : q8kv_quantize_kernel<kD, false>;
-  kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      x, out, n_tokens, heads, plane_stride, static_cast<int32_t>(tok_tiles),
-      static_cast<int32_t>(head_tiles));
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, x, out, n_tokens,
+                       heads, plane_stride, static_cast<int32_t>(tok_tiles), static_cast<int32_t>(head_tiles));
 }
 
 }  // namespace

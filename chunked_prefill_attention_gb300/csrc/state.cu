@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace q8a {
 namespace {
@@ -23,6 +24,8 @@ __host__ __device__ __forceinline__ int64_t i64min_host(int64_t a, int64_t b) { 
 __global__ void __launch_bounds__(kThreads)
 state_init_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
                   int64_t rows, int32_t head_dim) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   const int64_t start = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -39,6 +42,8 @@ __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4* __restrict__ out,
                 int64_t n_q, int32_t heads, int64_t row0, int64_t n_rows, int64_t rows) {
   // rows = B*H*n_rows state rows: query rows row0 .. row0+n_rows-1 of every plane
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int kParts = kD / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * kParts;
@@ -93,6 +98,8 @@ split_merge_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restr
                    const float* __restrict__ pm, const float* __restrict__ pl,
                    const float4* __restrict__ po, int64_t rows, int64_t n_q, int64_t q_pos0,
                    int64_t kv_start, int64_t split_keys, int32_t n_splits, int32_t causal) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * 8;
        g += stride) {
@@ -151,9 +158,8 @@ int grid_for(int64_t work) {
 cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, int32_t head_dim,
                               cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  state_init_kernel<<<grid_for(rows * (head_dim / 4)), kThreads, 0, stream>>>(
-      m, l, reinterpret_cast<float4*>(o), rows, head_dim);
-  return cudaGetLastError();
+  return launch_kernel(state_init_kernel, dim3(grid_for(rows * (head_dim / 4))), dim3(kThreads), 0, stream, m, l,
+                       reinterpret_cast<float4*>(o), rows, head_dim);
 }
 
 cudaError_t launch_finalize(const float* l, const float* o, void* out, int64_t batch,
@@ -168,20 +174,18 @@ cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int6
   if (rows <= 0) return cudaSuccess;
   if (head_dim != 64 && head_dim != 128) return cudaErrorInvalidValue;
   auto kernel = head_dim == 64 ? finalize_kernel<64> : finalize_kernel<128>;
-  kernel<<<grid_for(rows * (head_dim / 8)), kThreads, 0, stream>>>(
-      l, reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, row0,
-      n_rows, rows);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3(grid_for(rows * (head_dim / 8))), dim3(kThreads), 0, stream, l,
+                       reinterpret_cast<const float4*>(o), reinterpret_cast<uint4*>(out), n_q, heads, row0,
+                       n_rows, rows);
 }
 
 cudaError_t launch_split_merge(const ChunkArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.bh) * a.n_q;
   if (rows <= 0 || a.n_splits <= 0) return cudaSuccess;
-  split_merge_kernel<<<grid_for(rows * 8), kThreads, 0, stream>>>(
-      a.m, a.l, reinterpret_cast<float4*>(a.o), a.part_m, a.part_l,
-      reinterpret_cast<const float4*>(a.part_o), rows, a.n_q, a.q_pos0, a.kv_start, a.split_keys,
-      a.n_splits, a.causal);
-  return cudaGetLastError();
+  return launch_kernel(split_merge_kernel, dim3(grid_for(rows * 8)), dim3(kThreads), 0, stream, a.m, a.l,
+                       reinterpret_cast<float4*>(a.o), a.part_m, a.part_l,
+                       reinterpret_cast<const float4*>(a.part_o), rows, a.n_q, a.q_pos0, a.kv_start,
+                       a.split_keys, a.n_splits, a.causal);
 }
 
 }  // namespace q8a
