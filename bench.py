@@ -517,13 +517,14 @@ def run_burst(args):
     torch.cuda.empty_cache()
     st = Q.State(1, H, b.queries, dev, init=False)
     out = torch.empty((1, b.queries, H, b.head_dim), dtype=torch.float16, device=dev)
-    ws = torch.empty(Q.split_workspace_floats(1, H, b.queries, M, b.split_keys), dtype=torch.float32,
+    split = b.split_keys or Q.split_keys_for(H, M, torch.cuda.get_device_properties(dev).multi_processor_count)
+    ws = torch.empty(Q.split_workspace_floats(1, H, b.queries, M, split), dtype=torch.float32,
                      device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         Q.attn_state_init(st)
-        Q.attn_chunk_step_split(q, k8, v8, 0, M, st, b.split_keys, workspace=ws, q_pos0=M,
+        Q.attn_chunk_step_split(q, k8, v8, 0, M, st, split, workspace=ws, q_pos0=M,
                                 causal=False)
         Q.attn_finalize(st, out)
 
@@ -575,7 +576,7 @@ def run_burst(args):
         e2e = {"value": world * b.kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": int(qh.nbytes), "d2h_bytes_per_step": int(oh.nbytes)}
     config = {"workload": b.describe(), "batch": 1, "tokens": M, "queries": b.queries, "heads": H,
-              "head_dim": b.head_dim, "split_keys": b.split_keys, "replicas": world,
+              "head_dim": b.head_dim, "split_keys": split, "key_ranges": -(-M // split), "replicas": world,
               "l2": "Q8_0 KV %.2f GB, larger than L2" % (b.kv_bytes / 1e9)}
     extra = {
         "candidate_tokens_per_s": world * b.queries / (ms * 1e-3),

@@ -193,6 +193,24 @@ def split_workspace_floats(batch, heads, n_q, kv_len, split_keys):
     return n
 
 
+def split_keys_for(bh, kv_len, sms, max_waves=8, min_keys=2048):
+    """Key-range length for attn_chunk_step_split.  The split launch runs one
+    CTA per (batch, head) and key range, one CTA per SM, so the range count n
+    is chosen to make n * bh a whole number of waves: the fewest waves (up to
+    max_waves) whose CTA count bh divides, keeping ranges of at least min_keys
+    keys; the length is rounded up to whole 128-key tiles.  Without such a
+    count, ranges of 8,192 keys."""
+    if bh <= 0 or kv_len <= 0 or sms <= 0:
+        raise ValueError("bh, kv_len and sms must be positive")
+    for waves in range(1, max_waves + 1):
+        if (waves * sms) % bh == 0:
+            n = waves * sms // bh
+            length = -(-(-(-kv_len // n)) // 128) * 128
+            if length >= min_keys:
+                return length
+    return 8192
+
+
 def attn_chunk_step_split(q, k8, v8, kv_start, kv_len, state, split_keys, workspace=None, q_pos0=0,
                           scale=None, causal=True, stride=None, k_offset_bytes=0):
     """attn_chunk_step with the chunk's keys folded in parallel ranges of

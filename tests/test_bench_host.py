@@ -83,3 +83,23 @@ def test_step_bytes_of_the_smallest_workload():
     rows = 32 * 512
     chunks = sum(32 * (512 - s0) * 656 + 32 * 128 * 136 for s0 in (0, 128, 256, 384))
     assert bench.step_hbm_bytes(W.WORKLOADS["m512"]) == rows * (2 * 324 + 264 + 388) + chunks
+
+
+def test_split_keys_for_whole_waves():
+    """Range lengths for the split launch: whole waves of one CTA per SM."""
+    from chunked_prefill_attention_gb300.q8attn import split_keys_for
+    # 32 heads on 152 SMs: four waves = 608 CTAs = 19 ranges
+    n = split_keys_for(32, 1048576, 152)
+    assert n == 55296 and n % 128 == 0 and -(-1048576 // n) == 19
+    # one head on 152 SMs: one wave of 152 ranges
+    n = split_keys_for(1, 1048576, 152)
+    assert n % 128 == 0 and -(-1048576 // n) == 152
+    # 8 heads over 65,536 keys: one wave of 19 ranges of 3,456 keys
+    n = split_keys_for(8, 65536, 152)
+    assert n == 3456 and -(-65536 // n) * 8 == 152
+    # 9 heads: no whole number of waves within eight (152 w is a multiple of 9
+    # only from w = 9), and ranges that would be too short: 8,192
+    assert split_keys_for(9, 1 << 20, 152) == 8192
+    assert split_keys_for(1, 100000, 152) == 8192
+    with pytest.raises(ValueError):
+        split_keys_for(0, 10, 152)

@@ -141,8 +141,10 @@ def test_paired_launch_continues_a_state(lib, n_q, M, chunk):
 
 def test_burst_verification_bench_shape(lib):
     """The burst benchmark's own case: the 64 seeded candidates of the burst
-    workload against its 1,048,576-token, 32-head context, folded in key ranges
-    of 8,192 with a caller workspace, exactly as the benchmark launches it.
+    workload against its 1,048,576-token, 32-head context, folded in the key
+    ranges the benchmark picks (whole waves on this device: 19 ranges of 55,296
+    keys on 152 SMs) with a caller workspace, exactly as the benchmark launches
+    it.
     The oracle checks the Q8_0 bytes and the output of three of the heads."""
     from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
     from oracle import runner as oracle_runner
@@ -151,9 +153,10 @@ def test_burst_verification_bench_shape(lib):
     q, k, v = W.make_burst_inputs(b, device="cuda")
     k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
     st = Q.State(1, H, b.queries, q.device)
-    ws = torch.empty(Q.split_workspace_floats(1, H, b.queries, M, b.split_keys), dtype=torch.float32,
+    split = b.split_keys or Q.split_keys_for(H, M, torch.cuda.get_device_properties(0).multi_processor_count)
+    ws = torch.empty(Q.split_workspace_floats(1, H, b.queries, M, split), dtype=torch.float32,
                      device="cuda")
-    Q.attn_chunk_step_split(q, k8, v8, 0, M, st, b.split_keys, workspace=ws, q_pos0=M, causal=False)
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, st, split, workspace=ws, q_pos0=M, causal=False)
     out = Q.attn_finalize(st).cpu().numpy()
     assert_device_clean()
     heads = [0, 17, 31]
