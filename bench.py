@@ -464,20 +464,28 @@ def run_ours(args):
               % (2 * B * M * H * D * 4 / 1e9, B * M * H * D * 2 / 1e9, 2 * B * H * stride / 1e9,
                  (st.m.nbytes + st.l.nbytes + st.o.nbytes) / 1e9),
     }
+    attn_ms = chunk_ms + init_ms + fin_ms   # the step without the two quantise launches
     extra = {
         "tokens_per_s": tokens_s,
         "pct_fp16_peak": 100.0 * value / (world * peak_sus),
         "ms_attn_chunks_per_step": chunk_ms,
+        # the metric's own time base: every attn_chunk_step launch + init + finalise
+        "attention": {"ms_per_step": attn_ms, "tflops": flops / (attn_ms * 1e-3) / 1e12,
+                      "tokens_per_s": B * M / (attn_ms * 1e-3),
+                      "excludes": "the two q8kv_quantize launches (reported under quantize)"},
+        # one exponential per unmasked score, over the chunk launches
+        "exp_per_s": w.causal_pairs / (chunk_ms * 1e-3),
         "roofline": {"bound": "tensor", "kernel": "attn_chunk_step", "achieved": achieved,
                      "peak": peak_sus, "unit": UNIT, "frac": achieved / peak_sus,
                      "peak_kind": f"dense bf16/fp16 {peak_src} sustained (burst {peak_burst})",
                      "algorithmic": "4*D flops per unmasked (query, key) pair; %d launches/step" % launches_chunk,
                      "traffic": traffic, "traffic_note": traffic_state},
         "quantize": quantize_record(B, M, H, D, quant_ms, peaks, peak_src),
-        "state_init": hbm_record("attn_state_init", B * H * M * 264, init_ms, peaks, peak_src,
-                                 "264 B written per state row (m, l, 64 O)"),
-        "finalize": hbm_record("attn_finalize", B * H * M * 388, fin_ms, peaks, peak_src,
-                               "260 B read (l, 64 O) + 128 B fp16 written per state row"),
+        "state_init": hbm_record("attn_state_init", B * H * M * 4 * (2 + D), init_ms, peaks, peak_src,
+                                 "%d B written per state row (m, l, %d O)" % (4 * (2 + D), D)),
+        "finalize": hbm_record("attn_finalize", B * H * M * (4 * (1 + D) + 2 * D), fin_ms, peaks, peak_src,
+                               "%d B read (l, %d O) + %d B fp16 written per state row"
+                               % (4 * (1 + D), D, 2 * D)),
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": n_launch,
