@@ -33,9 +33,13 @@ int cuda_err(cudaError_t e, const char* what) {
 
 extern "C" {
 
+int64_t q8a_prefill_slot_floats_for(int64_t batch, int32_t heads, int64_t chunk, int32_t head_dim) {
+  if (batch < 0 || heads <= 0 || chunk <= 0 || (head_dim != 64 && head_dim != 128)) return -1;
+  return 4 * batch * chunk * heads * head_dim;   // 2 slots x (K, V) x [B][chunk][H][D]
+}
+
 int64_t q8a_prefill_slot_floats(int64_t batch, int32_t heads, int64_t chunk) {
-  if (batch < 0 || heads <= 0 || chunk <= 0) return -1;
-  return 4 * batch * chunk * heads * Q8A_HEAD_DIM;   // 2 slots x (K, V) x [B][chunk][H][64]
+  return q8a_prefill_slot_floats_for(batch, heads, chunk, Q8A_HEAD_DIM);
 }
 
 int attn_prefill_pipelined(const void* q_host, const float* k_host, const float* v_host,
@@ -45,28 +49,29 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
                            int64_t plane_stride_bytes, float* m, float* l, float* o, void* out_dev,
                            void* compute_stream, void* copy_stream) {
   q8a::NvtxRange nvtx_range("attn_prefill_pipelined");
-  if (batch < 0 || heads <= 0 || n_tokens < 0 || head_dim != Q8A_HEAD_DIM || chunk <= 0 ||
-      chunk % 4 != 0)
+  if (head_dim != 64 && head_dim != 128)
+    return q8a::set_error(Q8A_ERR_UNSUPPORTED, kFn, "head_dim must be 64 or 128");
+  if (batch < 0 || heads <= 0 || n_tokens < 0 || chunk <= 0 || chunk % 4 != 0)
     return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn,
-                          "sizes must be >= 0, heads > 0, head_dim 64 and chunk a positive "
-                          "multiple of 4");
+                          "sizes must be >= 0, heads > 0 and chunk a positive multiple of 4");
   if (batch == 0 || n_tokens == 0) return Q8A_OK;
   if (!q_host || !k_host || !v_host || !out_host || !q_dev || !kv_slots || !k8 || !v8 || !m ||
       !l || !o || !out_dev)
     return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn, "null pointer");
   // a chunk longer than the sequence only needs the sequence's tokens in a slot
   const int64_t slot_tokens = chunk < n_tokens ? chunk : n_tokens;
-  if (kv_slot_floats < q8a_prefill_slot_floats(batch, heads, slot_tokens))
+  if (kv_slot_floats < q8a_prefill_slot_floats_for(batch, heads, slot_tokens, head_dim))
     return q8a::set_error(Q8A_ERR_INVALID_ARG, kFn,
-                          "kv_slots holds fewer than q8a_prefill_slot_floats(batch, heads, "
-                          "min(chunk, n_tokens)) floats");
+                          "kv_slots holds fewer than q8a_prefill_slot_floats_for(batch, heads, "
+                          "min(chunk, n_tokens), head_dim) floats");
   if (reinterpret_cast<uintptr_t>(kv_slots) % 16 != 0)
     return q8a::set_error(Q8A_ERR_MISALIGNED, kFn, "kv_slots needs 16-byte alignment");
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
   cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
-  const int64_t row_floats = static_cast<int64_t>(heads) * Q8A_HEAD_DIM;   // one token, all heads
+  const int64_t row_floats = static_cast<int64_t>(heads) * head_dim;   // one token, all heads
+  const int64_t q8_row = head_dim / 32 * 34;                           // bytes of one Q8_0 head row
   // slot s holds K at kv_slots + 2*s*part and V at kv_slots + (2*s+1)*part, each
-  // [B][slot_tokens][H][64] (a shorter last chunk keeps the per-sequence stride)
+  // [B][slot_tokens][H][D] (a shorter last chunk keeps the per-sequence stride)
   const int64_t part = batch * slot_tokens * row_floats;
 
   // ev: a chunk's inputs are on the device (copy stream -> compute stream);
@@ -150,15 +155,15 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
     if ((e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess) return bail(cuda_err(e, "cudaStreamWaitEvent"));
     for (int64_t b = 0; b < batch; ++b) {
       const int64_t off = b * slot_tokens * row_floats;
-      uint8_t* kq = static_cast<uint8_t*>(k8) + b * heads * plane_stride_bytes + s0 * Q8A_ROW_BYTES;
-      uint8_t* vq = static_cast<uint8_t*>(v8) + b * heads * plane_stride_bytes + s0 * Q8A_ROW_BYTES;
+      uint8_t* kq = static_cast<uint8_t*>(k8) + b * heads * plane_stride_bytes + s0 * q8_row;
+      uint8_t* vq = static_cast<uint8_t*>(v8) + b * heads * plane_stride_bytes + s0 * q8_row;
       if ((rc = q8kv_quantize(ks + off, kq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK ||
           (rc = q8kv_quantize(vs + off, vq, 1, n, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK)
         return bail(rc);
     }
     if ((e = cudaEventRecord(ev_free[slot], cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
-    const uint8_t* kc = static_cast<const uint8_t*>(k8) + s0 * Q8A_ROW_BYTES;
-    const uint8_t* vc = static_cast<const uint8_t*>(v8) + s0 * Q8A_ROW_BYTES;
+    const uint8_t* kc = static_cast<const uint8_t*>(k8) + s0 * q8_row;
+    const uint8_t* vc = static_cast<const uint8_t*>(v8) + s0 * q8_row;
     if (c == 0) {
       for (int64_t r0 = 0; r0 < n_tokens; r0 += q_block) {
         const int64_t nr = (n_tokens - r0 < q_block) ? n_tokens - r0 : q_block;

@@ -51,6 +51,7 @@ SIGNATURES = {
     "attn_prefill_pipelined": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, _I64, _I32, _I64, _F, _I32,
                                               _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "q8a_prefill_slot_floats": (_I64, [_I64, _I32, _I64]),
+    "q8a_prefill_slot_floats_for": (_I64, [_I64, _I32, _I64, _I32]),
     "q8a_prefill_graph_create": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _I32,
                                                 _I64, _I32, _I64, _F, _I32, ctypes.POINTER(_P)]),
     "q8a_prefill_graph_launch": (ctypes.c_int, [_P, _P]),
@@ -310,19 +311,19 @@ class PipelineBuffers:
     Q and the output (whole sequence), two chunk slots of fp32 K and V, the
     Q8_0 planes of the whole sequence and the state."""
 
-    def __init__(self, batch, n_tokens, heads, device, chunk):
-        shape = (batch, n_tokens, heads, HEAD_DIM)
+    def __init__(self, batch, n_tokens, heads, device, chunk, head_dim=HEAD_DIM):
+        shape = (batch, n_tokens, heads, head_dim)
         self.chunk = chunk
         self.q = torch.empty(shape, dtype=torch.float16, device=device)
         self.out = torch.empty(shape, dtype=torch.float16, device=device)
-        n_slot = int(load().q8a_prefill_slot_floats(batch, heads, min(chunk, n_tokens)))
+        n_slot = int(load().q8a_prefill_slot_floats_for(batch, heads, min(chunk, n_tokens), head_dim))
         if n_slot < 0:
             raise Q8AttnError(Q8A_ERR_INVALID_ARG, "invalid sizes for the prefill slots")
         self.kv_slots = torch.empty((n_slot,), dtype=torch.float32, device=device)
-        self.stride = plane_stride(n_tokens)
+        self.stride = plane_stride(n_tokens, head_dim)
         self.k8 = torch.empty((batch, heads, self.stride), dtype=torch.uint8, device=device)
         self.v8 = torch.empty((batch, heads, self.stride), dtype=torch.uint8, device=device)
-        self.state = State(batch, heads, n_tokens, device, init=False)
+        self.state = State(batch, heads, n_tokens, device, init=False, head_dim=head_dim)
         self.copy_stream = torch.cuda.Stream(device=device)
 
 

@@ -25,8 +25,9 @@
  *     Q8A_ERR_INVALID_ARG.
  *   - head_dim D is 64 (two Q8_0 blocks per head row) for every call, and
  *     128 (four blocks) for q8kv_quantize, attn_state_init, attn_chunk_step,
- *     attn_chunk_step_gqa and attn_finalize; the split, allocation-free split
- *     and pipelined calls answer Q8A_ERR_UNSUPPORTED for 128.
+ *     attn_chunk_step_gqa, attn_finalize, attn_prefill_pipelined and the
+ *     captured prefill; the split and allocation-free split calls answer
+ *     Q8A_ERR_UNSUPPORTED for 128.
  *   - Layouts (all row-major, contiguous):
  *       Q, out    fp16  [B][n_q][H][D]           token-major
  *       x (K, V)  fp32  [B][n_tokens][H][D]      token-major
@@ -57,8 +58,9 @@ extern "C" {
  * split, allocation-free split, pipelined and grouped-query calls.  3: the
  * pipelined call streams K and V through two chunk slots (kv_slots).  4:
  * head_dim 128 and q8a_plane_stride_bytes_for.  5: the captured prefill
- * (q8a_prefill_graph_*). */
-#define Q8A_ABI_VERSION 5u
+ * (q8a_prefill_graph_*).  6: attn_prefill_pipelined at head_dim 128 and
+ * q8a_prefill_slot_floats_for. */
+#define Q8A_ABI_VERSION 6u
 
 enum {
   Q8A_OK = 0,
@@ -273,14 +275,16 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  * chunks; without it, attn_finalize and one copy back run at the end.  The
  * result is bit-identical to quantising the whole K and V, folding the same
  * chunks in order and finalising.
- *   q_host, out_host   fp16 [B][n_tokens][H][64] in host memory;
- *   k_host, v_host     fp32 [B][n_tokens][H][64] in host memory;
+ *   q_host, out_host   fp16 [B][n_tokens][H][D] in host memory (D = head_dim,
+ *                      64 or 128);
+ *   k_host, v_host     fp32 [B][n_tokens][H][D] in host memory;
  *                      page-locked host memory lets the copies overlap the
  *                      device work (pageable memory works, without overlap).
  *   q_dev, out_dev     device buffers of the layout and size of q_host;
  *   kv_slots           device fp32 scratch, 16-byte aligned, of at least
- *                      q8a_prefill_slot_floats(batch, heads, min(chunk,
- *                      n_tokens)) floats (kv_slot_floats); overwritten;
+ *                      q8a_prefill_slot_floats_for(batch, heads, min(chunk,
+ *                      n_tokens), head_dim) floats (kv_slot_floats);
+ *                      overwritten;
  *   k8, v8, plane_stride_bytes    the Q8_0 planes of the whole sequence (as for
  *                      q8kv_quantize): the cache this prefill produces;
  *   m, l, o            the state (as for attn_state_init; initialised here);
@@ -293,8 +297,8 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  *                      host once compute_stream has drained.
  * The call creates and releases five CUDA events; it allocates no memory.
  * Errors: Q8A_ERR_INVALID_ARG (sizes, null pointers, too small kv_slots),
- * Q8A_ERR_MISALIGNED, those of the calls above, Q8A_ERR_CUDA (a copy, event or
- * stream call failed).
+ * Q8A_ERR_UNSUPPORTED (head_dim), Q8A_ERR_MISALIGNED, those of the calls above,
+ * Q8A_ERR_CUDA (a copy, event or stream call failed).
  */
 int attn_prefill_pipelined(const void *q_host, const float *k_host, const float *v_host,
                            void *out_host, int64_t batch, int32_t heads, int64_t n_tokens,
@@ -303,9 +307,14 @@ int attn_prefill_pipelined(const void *q_host, const float *k_host, const float 
                            void *v8, int64_t plane_stride_bytes, float *m, float *l, float *o,
                            void *out_dev, void *compute_stream, void *copy_stream);
 
-/* Floats of kv_slots attn_prefill_pipelined needs: 4 * batch * chunk * heads * 64
- * (two slots of one chunk's fp32 K and V); -1 for invalid sizes. */
+/* Floats of kv_slots attn_prefill_pipelined needs at head_dim 64: 4 * batch *
+ * chunk * heads * 64 (two slots of one chunk's fp32 K and V); -1 for invalid
+ * sizes. */
 int64_t q8a_prefill_slot_floats(int64_t batch, int32_t heads, int64_t chunk);
+
+/* The same at head_dim 64 or 128: 4 * batch * chunk * heads * head_dim; -1 for
+ * invalid sizes or another head_dim. */
+int64_t q8a_prefill_slot_floats_for(int64_t batch, int32_t heads, int64_t chunk, int32_t head_dim);
 
 /*
  * q8a_prefill_graph_create -- capture one whole device-resident prefill into a

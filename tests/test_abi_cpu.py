@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), f"missing export {n}"
         assert n in q8attn.SIGNATURES, f"binding lacks {n}"
-    assert lib.q8a_abi_version() == 5
+    assert lib.q8a_abi_version() == 6
 
 
 def test_plane_stride(lib):
@@ -174,7 +174,12 @@ def test_pipelined_prefill_validation(lib):
     assert lib.q8a_prefill_slot_floats(1, 0, 100) == -1
     assert call(chunk=0) == Q.Q8A_ERR_INVALID_ARG
     assert call(chunk=6) == Q.Q8A_ERR_INVALID_ARG
-    assert call(hd=128) == Q.Q8A_ERR_INVALID_ARG
+    assert call(hd=32) == Q.Q8A_ERR_UNSUPPORTED
+    # head_dim 128 needs twice the slot floats of head_dim 64
+    assert call(hd=128) == Q.Q8A_ERR_INVALID_ARG and b"kv_slots" in lib.q8a_last_error()
+    assert lib.q8a_prefill_slot_floats_for(2, 3, 100, 128) == 4 * 2 * 100 * 3 * 128
+    assert lib.q8a_prefill_slot_floats_for(2, 3, 100, 64) == lib.q8a_prefill_slot_floats(2, 3, 100)
+    assert lib.q8a_prefill_slot_floats_for(2, 3, 100, 96) == -1
     assert call(q=P(0)) == Q.Q8A_ERR_INVALID_ARG
     assert call(slots=P(0)) == Q.Q8A_ERR_INVALID_ARG
     # two slots of one 256-token chunk are needed, whatever the sequence length
@@ -227,8 +232,8 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_head_dim_128_strides_and_unsupported_calls(lib):
-    """head_dim 128 rows are four 34-byte blocks; the split and pipelined calls
-    stay at head_dim 64."""
+    """head_dim 128 rows are four 34-byte blocks; the split calls stay at
+    head_dim 64."""
     from chunked_prefill_attention_gb300 import q8attn as Q
     assert lib.q8a_plane_stride_bytes_for(100, 128) == (100 * 136 + 15) // 16 * 16
     assert lib.q8a_plane_stride_bytes_for(100, 64) == lib.q8a_plane_stride_bytes(100)

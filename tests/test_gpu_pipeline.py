@@ -57,3 +57,27 @@ def test_pipelined_without_causal_mask(lib, B, M, H, chunk):
     assert torch.equal(oh, ref.cpu())
     want, *_ = oracle_out(q, k, v, causal=False)
     compare(oh.numpy(), want, f"pipelined non-causal B{B} M{M}")
+
+
+@pytest.mark.parametrize("B,M,H,chunk,causal", [(1, 1000, 2, 256, True), (2, 1800, 3, 512, True),
+                                                (1, 9000, 2, 4096, True), (1, 700, 2, 256, False)])
+def test_pipelined_head_dim_128(lib, B, M, H, chunk, causal):
+    """head_dim 128 (136-byte Q8_0 rows): slots of twice the floats, chunk 0's
+    query blocks folded by the two-query-tile kernel (and a one-tile last
+    block by the paired kernel), bit-identical to the device path."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    D = 128
+    q = seeded((B, M, H, D), M + 91, "cuda", torch.float16)
+    k = seeded((B, M, H, D), M + 92, "cuda")
+    v = seeded((B, M, H, D), M + 93, "cuda")
+    ref, *_ = Q.prefill_attention(q, k, v, chunk, causal=causal)
+    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    oh = torch.zeros((B, M, H, D), dtype=torch.float16).pin_memory()
+    bufs = Q.PipelineBuffers(B, M, H, q.device, chunk, head_dim=D)
+    assert bufs.kv_slots.numel() == 4 * B * min(chunk, M) * H * D
+    Q.attn_prefill_pipelined(qh, kh, vh, oh, bufs, causal=causal)
+    torch.cuda.current_stream().synchronize()
+    assert_device_clean()
+    assert torch.equal(oh, ref.cpu())
+    want, *_ = oracle_out(q, k, v, causal=causal)
+    compare(oh.numpy(), want, f"pipelined d128 B{B} M{M} causal {causal}")
