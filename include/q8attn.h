@@ -233,8 +233,7 @@ int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, in
  *   key ranges or attn_chunk_step_split with a workspace of your own.
  *   The first call on a device looks up the scratch's device address on that
  *   (current) device, and looks it up again when the device's context has
- *   changed since (after cudaDeviceReset); make the first call before any
- *   stream capture.
+ *   changed since (after cudaDeviceReset).
  *   Every call on a device shares the one scratch array, which keeps the last
  *   call's contents; each call writes every partial it later reads, so no
  *   clearing is needed, but calls whose kernels can overlap on the GPU (other
