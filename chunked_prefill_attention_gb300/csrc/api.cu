@@ -303,11 +303,18 @@ int q8a::chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const
 
 extern "C" {
 
+int64_t q8a_split_workspace_floats_for(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
+                                       int64_t split_keys, int32_t head_dim) {
+  if (batch < 0 || heads <= 0 || n_q < 0 || kv_len < 0 || split_keys <= 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return -1;
+  const int64_t n_splits = (kv_len + split_keys - 1) / split_keys;
+  return n_splits * batch * heads * n_q * (head_dim + 2);
+}
+
 int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
                                    int64_t split_keys) {
-  if (batch < 0 || heads <= 0 || n_q < 0 || kv_len < 0 || split_keys <= 0) return -1;
-  const int64_t n_splits = (kv_len + split_keys - 1) / split_keys;
-  return n_splits * batch * heads * n_q * (Q8A_HEAD_DIM + 2);
+  return q8a_split_workspace_floats_for(batch, heads, n_q, kv_len, split_keys, Q8A_HEAD_DIM);
 }
 
 int attn_chunk_step_gqa(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
@@ -342,8 +349,8 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
                           float* workspace, int64_t workspace_floats, void* stream) {
   q8a::NvtxRange nvtx_range("attn_chunk_step_split");
   const char* fn = "attn_chunk_step_split";
-  if (head_dim != Q8A_HEAD_DIM)
-    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 (got %d)", fn, head_dim);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 or 128 (got %d)", fn, head_dim);
   if (split_keys <= 0 || split_keys % 128 != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
                 fn, (long long)split_keys);
@@ -353,7 +360,7 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
     n_splits = (kv_len + split_keys - 1) / split_keys;
     if (n_splits > 65535) return fail(Q8A_ERR_UNSUPPORTED, "%s: more than 65535 key ranges", fn);
     rows = batch * heads * n_q;
-    const int64_t need = n_splits * rows * (Q8A_HEAD_DIM + 2);
+    const int64_t need = n_splits * rows * (head_dim + 2);
     if (!workspace) return fail(Q8A_ERR_INVALID_ARG, "%s: null workspace", fn);
     if (workspace_floats < need)
       return fail(Q8A_ERR_INVALID_ARG, "%s: workspace of %lld floats < %lld needed", fn,
@@ -369,15 +376,15 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
                                   &qmap, &a, &empty))
     return rc;
   if (empty) return ok();
-  // workspace: partial O [n_splits][rows][64], then m [n_splits][rows], then l
+  // workspace: partial O [n_splits][rows][D], then m [n_splits][rows], then l
   a.split_keys = split_keys;
   a.n_splits = static_cast<int32_t>(n_splits);
   a.part_o = workspace;
-  a.part_m = workspace + n_splits * rows * Q8A_HEAD_DIM;
+  a.part_m = workspace + n_splits * rows * head_dim;
   a.part_l = a.part_m + n_splits * rows;
   a.inject = g_inject.exchange(0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = q8a::launch_chunk_step(qmap, a, st);
+  cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, st) : q8a::launch_chunk_step(qmap, a, st);
   if (e == cudaSuccess) e = q8a::launch_split_merge(a, st);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
@@ -456,14 +463,14 @@ int attn_chunk_step_split_static(const void* q, int64_t q_pos0, const void* k_q8
                                  int64_t split_keys, void* stream) {
   q8a::NvtxRange nvtx_range("attn_chunk_step_split_static");
   const char* fn = "attn_chunk_step_split_static";
-  if (head_dim != Q8A_HEAD_DIM)
-    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 (got %d)", fn, head_dim);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 or 128 (got %d)", fn, head_dim);
   if (split_keys <= 0 || split_keys % 128 != 0)
     return fail(Q8A_ERR_INVALID_ARG, "%s: split_keys must be a positive multiple of 128 (got %lld)",
                 fn, (long long)split_keys);
   float* ws = nullptr;
   if (batch > 0 && heads > 0 && n_q > 0 && kv_len > 0) {
-    const int64_t need = q8a_split_workspace_floats(batch, heads, n_q, kv_len, split_keys);
+    const int64_t need = q8a_split_workspace_floats_for(batch, heads, n_q, kv_len, split_keys, head_dim);
     if (need > kStaticSplitFloats)
       return fail(Q8A_ERR_INVALID_ARG,
                   "%s: the partial states need %lld floats, more than the %lld of the static "

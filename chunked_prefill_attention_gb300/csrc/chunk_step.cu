@@ -977,7 +977,34 @@ struct Unit {
   int T_all;
 };
 
-__device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
+// The chunk, or in the split form this CTA's key range and its partial state
+// (as at head_dim 64, with 136-byte rows and 128-channel O rows).
+__device__ __forceinline__ Range make_range(const ChunkArgs& a) {
+  Range r;
+  r.kv_len = a.kv_len;
+  r.kv_start = a.kv_start;
+  r.k8 = a.k8;
+  r.v8 = a.v8;
+  r.m = a.m;
+  r.l = a.l;
+  r.o = a.o;
+  r.fresh = false;
+  if (a.split_keys > 0) {
+    const int64_t off = static_cast<int64_t>(blockIdx.y) * a.split_keys;
+    const int64_t rows = static_cast<int64_t>(a.bh) * a.n_q;
+    r.kv_len = i64min(a.split_keys, a.kv_len - off);
+    r.kv_start = a.kv_start + off;
+    r.k8 = a.k8 + off * ROWB;
+    r.v8 = a.v8 + off * ROWB;
+    r.m = a.part_m + blockIdx.y * rows;
+    r.l = a.part_l + blockIdx.y * rows;
+    r.o = a.part_o + blockIdx.y * rows * D;
+    r.fresh = true;
+  }
+  return r;
+}
+
+__device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
   const int64_t idx = blockIdx.x;
   u.bh = idx / a.n_qtiles;
@@ -985,10 +1012,10 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
   u.b = u.bh / a.heads;
   u.h = u.bh % a.heads;
   u.r0 = (static_cast<int64_t>(a.tile0) + qt) * BM;
-  int64_t n_vis = a.kv_len;
+  int64_t n_vis = kr.kv_len;
   if (a.causal) {
     const int64_t r_last = i64min(u.r0 + BM - 1, a.n_q - 1);
-    n_vis = i64min(n_vis, a.q_pos0 + r_last - a.kv_start + 1);
+    n_vis = i64min(n_vis, a.q_pos0 + r_last - kr.kv_start + 1);
   }
   const int tiles = n_vis > 0 ? static_cast<int>((n_vis + BN - 1) / BN) : 0;
   u.T[0] = (tiles + 1) / 2;
@@ -997,8 +1024,8 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
   return u;
 }
 
-__device__ __forceinline__ void producer(const CUtensorMap* qmap, const ChunkArgs& a, const Unit& u,
-                                         uint8_t* smem, uint32_t sbase, Ctl* ctl) {
+__device__ __forceinline__ void producer(const CUtensorMap* qmap, const ChunkArgs& a, const Range& kr,
+                                         const Unit& u, uint8_t* smem, uint32_t sbase, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
@@ -1018,13 +1045,13 @@ __device__ __forceinline__ void producer(const CUtensorMap* qmap, const ChunkArg
 #pragma unroll
   for (int s = 0; s < NR; ++s) last_bulk[s] = -1;
   const int64_t kv_plane = u.b * a.kv_heads + u.h / (a.heads / a.kv_heads);
-  const uint8_t* kp = a.k8 + kv_plane * a.plane_stride;
-  const uint8_t* vp = a.v8 + kv_plane * a.plane_stride;
+  const uint8_t* kp = kr.k8 + kv_plane * a.plane_stride;
+  const uint8_t* vp = kr.v8 + kv_plane * a.plane_stride;
   for (int t = 0; t < u.T_all; ++t) {
     const int sr = t % NR;
     if (!wait_bar(bar(B_RAWEMPTY + sr), ((t / NR) & 1) ^ 1, ctl, budget, R_PRODUCER, true)) break;
     const int64_t k0 = static_cast<int64_t>(t) * BN;
-    const int n = static_cast<int>(i64min(BN, a.kv_len - k0));
+    const int n = static_cast<int>(i64min(BN, kr.kv_len - k0));
     const uint32_t bytes = static_cast<uint32_t>(n) * ROWB;
     const uint32_t dk = sbase + OFF_RAW + sr * 2 * RAWB;
     if ((bytes & 15u) == 0u) {
@@ -1063,7 +1090,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* qmap, const ChunkArg
 // Thread k < 64: K row k of each tile; thread 64 + k: V row k.  Block b of a
 // 136-byte row (channels 32b .. 32b+31) lands in atom column b / 2, 16-byte
 // chunks 4 (b % 2) .. 4 (b % 2) + 3 of the key's 128-byte row, swizzled.
-__device__ __forceinline__ void dequant(const ChunkArgs& a, const Unit& u, uint8_t* smem,
+__device__ __forceinline__ void dequant(const ChunkArgs& a, const Range& kr, const Unit& u, uint8_t* smem,
                                         uint32_t sbase, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;
   const int tid = threadIdx.x - 256;
@@ -1077,7 +1104,7 @@ __device__ __forceinline__ void dequant(const ChunkArgs& a, const Unit& u, uint8
     const uint32_t fill = static_cast<uint32_t>((t >> 1) & 1);
     if (!wait_bar(bar(B_RAWFULL + sr), (t / NR) & 1, ctl, budget, R_DEQUANT, true)) break;
     if (!wait_bar(bar((tensor ? B_VEMPTY : B_KEMPTY) + sd), fill ^ 1, ctl, budget, R_DEQUANT, true)) break;
-    const int n_valid = static_cast<int>(i64min(BN, a.kv_len - static_cast<int64_t>(t) * BN));
+    const int n_valid = static_cast<int>(i64min(BN, kr.kv_len - static_cast<int64_t>(t) * BN));
     uint8_t* hi = smem + OFF_DEQ + sd * DEQ_BYTES + (tensor ? DQ_VHI : DQ_KHI) + k * 128;
     uint8_t* lo = smem + OFF_DEQ + sd * DEQ_BYTES + (tensor ? DQ_VLO : DQ_KLO) + k * 128;
     if (k < n_valid) {
@@ -1233,8 +1260,8 @@ __device__ __forceinline__ void scale_o(uint32_t t_o, float alpha) {
   }
 }
 
-__device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x, uint8_t* smem,
-                                        uint32_t sbase, uint32_t tmem, Ctl* ctl) {
+__device__ __forceinline__ void softmax(const ChunkArgs& a, const Range& kr, const Unit& u, int x,
+                                        uint8_t* smem, uint32_t sbase, uint32_t tmem, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;
   const int row = threadIdx.x & 127;
   const int wq = (threadIdx.x >> 5) & 3;
@@ -1244,23 +1271,25 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
   if (T == 0) return;
   const int64_t rg = u.r0 + row;
   const int64_t pos = a.q_pos0 + rg;
-  const bool active = rg < a.n_q && (!a.causal || pos >= a.kv_start);
+  const bool active = rg < a.n_q && (!a.causal || pos >= kr.kv_start);
   const int64_t sidx = u.bh * a.n_q + rg;
   const uint32_t t_s = tmem + lane_off + T_S + 64u * x;
   const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
-  const bool fresh = x == 1;   // pipeline B starts empty; A merges it in at the end
+  // pipeline B starts empty and A merges it in at the end; in the split form
+  // both start empty (the partial state of this key range)
+  const bool fresh = kr.fresh || x == 1;
   const bool pair_merge = u.T[1] > 0;
   float m_run = -INFINITY, l_run = 0.0f;
   if (active && !fresh) {
-    m_run = a.m[sidx];
-    l_run = a.l[sidx];
+    m_run = kr.m[sidx];
+    l_run = kr.l[sidx];
   }
   {
     uint32_t oh[64];
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       if (active && !fresh) {
-        const float4* src = reinterpret_cast<const float4*>(a.o + sidx * D + 64 * hh);
+        const float4* src = reinterpret_cast<const float4*>(kr.o + sidx * D + 64 * hh);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float4 p = src[i];
@@ -1294,10 +1323,10 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
     wait_ld_at<0>(s);
     wait_ld_at<32>(s);
     const int64_t k0 = static_cast<int64_t>(2 * t + x) * BN;
-    const bool need_mask = (k0 + BN > a.kv_len) || (a.causal && a.kv_start + k0 + BN - 1 > q_first);
+    const bool need_mask = (k0 + BN > kr.kv_len) || (a.causal && kr.kv_start + k0 + BN - 1 > q_first);
     if (__builtin_expect(need_mask, 0)) {
-      int64_t lim = a.kv_len - 1 - k0;
-      if (a.causal) lim = i64min(lim, pos - a.kv_start - k0);
+      int64_t lim = kr.kv_len - 1 - k0;
+      if (a.causal) lim = i64min(lim, pos - kr.kv_start - k0);
       const int li = static_cast<int>(i64max(-1, i64min(lim, BN - 1)));
 #pragma unroll
       for (int j = 0; j < 64; ++j)
@@ -1366,8 +1395,8 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
   const float wa = (m_run == m) ? 1.0f : (m_run == -INFINITY ? 0.0f : ex2_approx((m_run - m) * kLog2e));
   const float wb = (m_b == m) ? 1.0f : (m_b == -INFINITY ? 0.0f : ex2_approx((m_b - m) * kLog2e));
   if (active) {
-    a.m[sidx] = m;
-    a.l[sidx] = pair_merge ? fmaf(wa, l_run, wb * l_b) : l_run;
+    kr.m[sidx] = m;
+    kr.l[sidx] = pair_merge ? fmaf(wa, l_run, wb * l_b) : l_run;
   }
 #pragma unroll 1
   for (int q = 0; q < 4; ++q) {   // 32 channels at a time
@@ -1377,7 +1406,7 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
     tmem_wait_ld(oa);
     if (pair_merge) tmem_wait_ld(ob);
     if (active) {
-      float4* dst = reinterpret_cast<float4*>(a.o + sidx * D + 32 * q);
+      float4* dst = reinterpret_cast<float4*>(kr.o + sidx * D + 32 * q);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float v[4];
@@ -1404,7 +1433,8 @@ chunk_step_d128_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + OFF_CTL);
   const int warp = threadIdx.x >> 5;
   const int wg = warp >> 2;
-  const Unit u = make_unit(a);
+  const Range kr = d128::make_range(a);
+  const Unit u = d128::make_unit(a, kr);
   if (u.T_all == 0) return;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
@@ -1429,13 +1459,13 @@ chunk_step_d128_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs
   const uint32_t tmem = ctl->tmem_base;
   if (wg < 2) {
     reg_alloc<kRegSoftmax>();
-    softmax(a, u, wg, smem, sbase, tmem, ctl);
+    softmax(a, kr, u, wg, smem, sbase, tmem, ctl);
   } else {
     reg_dealloc<kRegOther>();
     if (wg == 2) {
-      dequant(a, u, smem, sbase, ctl);
+      dequant(a, kr, u, smem, sbase, ctl);
     } else if (warp == 12) {
-      producer(&qmap, a, u, smem, sbase, ctl);
+      producer(&qmap, a, kr, u, smem, sbase, ctl);
     } else if (warp == 13) {
       mma(a, u, sbase, tmem, ctl);
     }
@@ -2006,7 +2036,7 @@ cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& arg
     }
     configured_device = dev;
   }
-  if (args.n_qtiles >= 2) {
+  if (args.n_qtiles >= 2 && args.split_keys == 0) {
     // two query tiles per CTA, Q in TMEM
     static thread_local int configured_x2 = -1;
     if (configured_x2 != dev) {
@@ -2033,11 +2063,13 @@ cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& arg
                       d128x2::kThreads, d128x2::SMEM_BYTES);
     return e;
   }
-  // a single query tile: both pipelines on its rows (paired)
+  // a single query tile, or the split form: one query tile per CTA, both
+  // pipelines on its rows (paired); the split form adds a grid row per key range
   const int64_t blocks = static_cast<int64_t>(args.n_qtiles) * args.bh;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  e = launch_kernel(d128::chunk_step_d128_kernel, dim3(static_cast<unsigned>(blocks)), dim3(d128::kThreads),
+  const unsigned gy = args.split_keys > 0 ? static_cast<unsigned>(args.n_splits) : 1u;
+  e = launch_kernel(d128::chunk_step_d128_kernel, dim3(static_cast<unsigned>(blocks), gy), dim3(d128::kThreads),
                     d128::SMEM_BYTES, stream, qmap, args);
   if (e != cudaSuccess)
     set_launch_note("chunk_step_d128_kernel<<<%lld, %d, %d>>>", static_cast<long long>(blocks),

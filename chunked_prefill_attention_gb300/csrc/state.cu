@@ -86,13 +86,14 @@ finalize_kernel(const float* __restrict__ l, const float4* __restrict__ o, uint4
   }
 }
 
-// Merge of the split partial states into the state, one (b, h, row) per 8
+// Merge of the split partial states into the state, one (b, h, row) per kD / 8
 // threads (8 channels each).  It is the chunk recurrence applied with a
 // partial's (m_s, l_s, O_s) in place of a chunk's row max, weight sum and
 // weighted values:  m' = max(m, m_s...),  l' = l e^(m - m') + sum_s l_s e^(m_s - m'),
 // O' = O e^(m - m') + sum_s O_s e^(m_s - m').  A partial is read only when its
 // key range holds a key the row can see (the chunk-step kernel writes exactly
 // those rows).
+template <int kD>
 __global__ void __launch_bounds__(kThreads)
 split_merge_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
                    const float* __restrict__ pm, const float* __restrict__ pl,
@@ -101,10 +102,12 @@ split_merge_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restr
   pdl_launch_dependents();
   pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * 8;
+  constexpr int kParts = kD / 8;      // threads per row (8 or 16: a row never spans two warps)
+  constexpr int kRowF4 = kD / 4;      // float4 per O row
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < rows * kParts;
        g += stride) {
-    const int64_t row = g >> 3;   // (b*H + h)*n_q + r
-    const int part = static_cast<int>(g & 7);
+    const int64_t row = g / kParts;   // (b*H + h)*n_q + r
+    const int part = static_cast<int>(g % kParts);
     const int64_t pos = q_pos0 + row % n_q;
     // splits whose first key the row can see (all of them without the mask)
     int ns = n_splits;
@@ -120,24 +123,24 @@ split_merge_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restr
     if (mx == -INFINITY) continue;
     const float f = (m0 == -INFINITY) ? 0.0f : expf(m0 - mx);
     float lv = l0 * f;
-    float4 a = o[row * 16 + 2 * part], c = o[row * 16 + 2 * part + 1];
+    float4 a = o[row * kRowF4 + 2 * part], c = o[row * kRowF4 + 2 * part + 1];
     float y[8] = {a.x * f, a.y * f, a.z * f, a.w * f, c.x * f, c.y * f, c.z * f, c.w * f};
     for (int s = 0; s < ns; ++s) {
       const float ms = pm[s * rows + row];
       if (ms == -INFINITY) continue;
       const float w = expf(ms - mx);
       lv = fmaf(pl[s * rows + row], w, lv);
-      const float4 pa = po[(s * rows + row) * 16 + 2 * part];
-      const float4 pc = po[(s * rows + row) * 16 + 2 * part + 1];
+      const float4 pa = po[(s * rows + row) * kRowF4 + 2 * part];
+      const float4 pc = po[(s * rows + row) * kRowF4 + 2 * part + 1];
       y[0] = fmaf(pa.x, w, y[0]); y[1] = fmaf(pa.y, w, y[1]);
       y[2] = fmaf(pa.z, w, y[2]); y[3] = fmaf(pa.w, w, y[3]);
       y[4] = fmaf(pc.x, w, y[4]); y[5] = fmaf(pc.y, w, y[5]);
       y[6] = fmaf(pc.z, w, y[6]); y[7] = fmaf(pc.w, w, y[7]);
     }
-    o[row * 16 + 2 * part] = make_float4(y[0], y[1], y[2], y[3]);
-    o[row * 16 + 2 * part + 1] = make_float4(y[4], y[5], y[6], y[7]);
-    // the row's eight lanes took the same path; all have read m and l by now
-    __syncwarp(0xFFu << ((threadIdx.x & 31) & ~7));
+    o[row * kRowF4 + 2 * part] = make_float4(y[0], y[1], y[2], y[3]);
+    o[row * kRowF4 + 2 * part + 1] = make_float4(y[4], y[5], y[6], y[7]);
+    // the row's lanes took the same path; all have read m and l by now
+    __syncwarp(((1u << kParts) - 1u) << ((threadIdx.x & 31) & ~(kParts - 1)));
     if (part == 0) {
       m[row] = mx;
       l[row] = lv;
@@ -182,7 +185,9 @@ cudaError_t launch_finalize_rows(const float* l, const float* o, void* out, int6
 cudaError_t launch_split_merge(const ChunkArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.bh) * a.n_q;
   if (rows <= 0 || a.n_splits <= 0) return cudaSuccess;
-  return launch_kernel(split_merge_kernel, dim3(grid_for(rows * 8)), dim3(kThreads), 0, stream, a.m, a.l,
+  if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
+  auto kernel = a.head_dim == 64 ? split_merge_kernel<64> : split_merge_kernel<128>;
+  return launch_kernel(kernel, dim3(grid_for(rows * (a.head_dim / 8))), dim3(kThreads), 0, stream, a.m, a.l,
                        reinterpret_cast<float4*>(a.o), a.part_m, a.part_l,
                        reinterpret_cast<const float4*>(a.part_o), rows, a.n_q, a.q_pos0, a.kv_start,
                        a.split_keys, a.n_splits, a.causal);

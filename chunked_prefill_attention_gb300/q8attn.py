@@ -44,6 +44,7 @@ SIGNATURES = {
     "attn_chunk_step_split": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
                                              _I32, _I64, _I32, _F, _I32, _I64, _P, _I64, _P]),
     "q8a_split_workspace_floats": (_I64, [_I64, _I32, _I64, _I64, _I64]),
+    "q8a_split_workspace_floats_for": (_I64, [_I64, _I32, _I64, _I64, _I64, _I32]),
     "attn_chunk_step_split_static": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P,
                                                     _I64, _I32, _I64, _I32, _F, _I32, _I64, _P]),
     "q8a_static_split_scratch_floats": (_I64, []),
@@ -187,8 +188,8 @@ def attn_chunk_step_gqa(q, k8, v8, kv_start, kv_len, state, q_pos0=0, scale=None
     return state
 
 
-def split_workspace_floats(batch, heads, n_q, kv_len, split_keys):
-    n = int(load().q8a_split_workspace_floats(batch, heads, n_q, kv_len, split_keys))
+def split_workspace_floats(batch, heads, n_q, kv_len, split_keys, head_dim=HEAD_DIM):
+    n = int(load().q8a_split_workspace_floats_for(batch, heads, n_q, kv_len, split_keys, head_dim))
     if n < 0:
         raise Q8AttnError(Q8A_ERR_INVALID_ARG, "invalid sizes for the split workspace")
     return n
@@ -222,7 +223,7 @@ def attn_chunk_step_split(q, k8, v8, kv_start, kv_len, state, split_keys, worksp
         scale = 1.0 / math.sqrt(D)
     if stride is None:
         stride = k8.shape[-1]
-    need = split_workspace_floats(B, H, n_q, kv_len, split_keys)
+    need = split_workspace_floats(B, H, n_q, kv_len, split_keys, D)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.float32, device=q.device)
     lib = load()

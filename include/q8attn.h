@@ -25,9 +25,8 @@
  *     Q8A_ERR_INVALID_ARG.
  *   - head_dim D is 64 (two Q8_0 blocks per head row) for every call, and
  *     128 (four blocks) for q8kv_quantize, attn_state_init, attn_chunk_step,
- *     attn_chunk_step_gqa, attn_finalize, attn_prefill_pipelined and the
- *     captured prefill; the split and allocation-free split calls answer
- *     Q8A_ERR_UNSUPPORTED for 128.
+ *     attn_chunk_step_gqa, attn_chunk_step_split (and its allocation-free
+ *     form), attn_finalize, attn_prefill_pipelined and the captured prefill.
  *   - Layouts (all row-major, contiguous):
  *       Q, out    fp16  [B][n_q][H][D]           token-major
  *       x (K, V)  fp32  [B][n_tokens][H][D]      token-major
@@ -58,8 +57,8 @@ extern "C" {
  * split, allocation-free split, pipelined and grouped-query calls.  3: the
  * pipelined call streams K and V through two chunk slots (kv_slots).  4:
  * head_dim 128 and q8a_plane_stride_bytes_for.  5: the captured prefill
- * (q8a_prefill_graph_*).  6: attn_prefill_pipelined at head_dim 128 and
- * q8a_prefill_slot_floats_for. */
+ * (q8a_prefill_graph_*).  6: attn_prefill_pipelined and the split calls at
+ * head_dim 128, q8a_prefill_slot_floats_for and q8a_split_workspace_floats_for. */
 #define Q8A_ABI_VERSION 6u
 
 enum {
@@ -189,9 +188,12 @@ int attn_chunk_step_gqa(const void *q, int64_t q_pos0, const void *k_q8, const v
  * up to floating-point rounding.  Arguments as for attn_chunk_step, plus:
  *   split_keys        keys per range, a positive multiple of 128.
  *   workspace         caller-owned fp32 scratch, 16-byte aligned, of at least
- *                     q8a_split_workspace_floats(batch, heads, n_q, kv_len,
- *                     split_keys) floats; its contents are overwritten.  Calls
- *                     sharing one workspace must be ordered on one stream.
+ *                     q8a_split_workspace_floats_for(batch, heads, n_q, kv_len,
+ *                     split_keys, head_dim) floats; its contents are
+ *                     overwritten.  Calls sharing one workspace must be ordered
+ *                     on one stream.
+ * At head_dim 128 each key range is folded by the paired kernel (one 128-row
+ * query tile per CTA, its two pipelines on alternate 64-key tiles).
  *   workspace_floats  its size in floats.
  * Two kernel launches on `stream`.  Errors: as attn_chunk_step; Q8A_ERR_INVALID_ARG
  * also for a bad split_keys or a missing or too small workspace;
@@ -208,10 +210,15 @@ int attn_chunk_step_split(const void *q, int64_t q_pos0, const void *k_q8, const
                           int64_t split_keys, float *workspace, int64_t workspace_floats,
                           void *stream);
 
-/* Floats of workspace attn_chunk_step_split needs:
+/* Floats of workspace attn_chunk_step_split needs at head_dim 64:
  * ceil(kv_len / split_keys) * batch * heads * n_q * 66; -1 for invalid sizes. */
 int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
                                    int64_t split_keys);
+
+/* The same at head_dim 64 or 128: ceil(kv_len / split_keys) * batch * heads *
+ * n_q * (head_dim + 2); -1 for invalid sizes or another head_dim. */
+int64_t q8a_split_workspace_floats_for(int64_t batch, int32_t heads, int64_t n_q, int64_t kv_len,
+                                       int64_t split_keys, int32_t head_dim);
 
 /*
  * attn_chunk_step_split_static -- attn_chunk_step_split for callers that
@@ -228,7 +235,7 @@ int64_t q8a_split_workspace_floats(int64_t batch, int32_t heads, int64_t n_q, in
  * part of the method.
  *   Arguments, result and errors: as attn_chunk_step_split without the
  *   workspace.  A call whose partial states would need more floats than the
- *   scratch holds (q8a_split_workspace_floats(...) > the scratch size) is
+ *   scratch holds (q8a_split_workspace_floats_for(...) > the scratch size) is
  *   rejected with Q8A_ERR_INVALID_ARG before anything is launched; use larger
  *   key ranges or attn_chunk_step_split with a workspace of your own.
  *   The first call on a device looks up the scratch's device address on that

@@ -231,18 +231,27 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         q8attn.load()
 
 
-def test_head_dim_128_strides_and_unsupported_calls(lib):
-    """head_dim 128 rows are four 34-byte blocks; the split calls stay at
-    head_dim 64."""
+def test_head_dim_128_strides_and_split_sizes(lib):
+    """head_dim 128 rows are four 34-byte blocks; the split calls size their
+    partial states by the head dimension and check the workspace before any
+    CUDA call."""
     from chunked_prefill_attention_gb300 import q8attn as Q
     assert lib.q8a_plane_stride_bytes_for(100, 128) == (100 * 136 + 15) // 16 * 16
     assert lib.q8a_plane_stride_bytes_for(100, 64) == lib.q8a_plane_stride_bytes(100)
     assert lib.q8a_plane_stride_bytes_for(100, 96) == -1
     assert lib.q8a_plane_stride_bytes_for(-1, 128) == -1
+    need = lib.q8a_split_workspace_floats_for(1, 2, 64, 512, 128, 128)
+    assert need == 4 * 1 * 2 * 64 * 130
+    assert lib.q8a_split_workspace_floats_for(1, 2, 64, 512, 128, 64) == lib.q8a_split_workspace_floats(1, 2, 64, 512, 128)
+    assert lib.q8a_split_workspace_floats_for(1, 2, 64, 512, 128, 96) == -1
     s = P(0)
-    rc = lib.attn_chunk_step_split(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64, 128,
+    rc = lib.attn_chunk_step_split(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64, 96,
                                    0.125, 0, 128, A16, 1 << 20, s)
     assert rc == Q.Q8A_ERR_UNSUPPORTED and b"head_dim" in lib.q8a_last_error()
+    # enough for head_dim 64 but not for 128
+    rc = lib.attn_chunk_step_split(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64, 128,
+                                   0.125, 0, 128, A16, lib.q8a_split_workspace_floats(1, 2, 64, 512, 128), s)
+    assert rc == Q.Q8A_ERR_INVALID_ARG and b"workspace" in lib.q8a_last_error()
     rc = lib.attn_chunk_step_split_static(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64,
-                                          128, 0.125, 0, 128, s)
+                                          96, 0.125, 0, 128, s)
     assert rc == Q.Q8A_ERR_UNSUPPORTED

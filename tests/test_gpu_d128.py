@@ -109,3 +109,59 @@ def test_d128_chunk_order(lib):
     for order in ([0, 1, 2], [2, 0, 1]):
         out, *_ = run_gpu(q, k, v, 256, order=order)
         compare(out.cpu().numpy(), want, f"d128 order {order}")
+
+
+@pytest.mark.parametrize("M,H,split", [(4096, 4, 512), (3000, 2, 384), (20000, 8, 2048)])
+def test_d128_burst_split(lib, M, H, split):
+    """Burst verification at head_dim 128: 64 candidates after the context,
+    no mask, the keys folded in parallel ranges (the paired kernel per range)
+    and merged."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    q, k, v = _inputs(1, M, H, seed=M + split, n_q=64)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, 64, q.device, head_dim=D)
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, st, split, q_pos0=M, causal=False)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want, *_ = oracle_out(q, k, v, causal=False, q_pos0=M)
+    compare(out.cpu().numpy(), want, f"d128 burst M{M} split{split}")
+
+
+@pytest.mark.parametrize("M,chunk,split", [(1000, 1000, 256), (1030, 512, 128)])
+def test_d128_causal_split(lib, M, chunk, split):
+    """Causal prefill with every chunk split at head_dim 128: later ranges are
+    invisible to the early rows of a chunk, whose partials the merge skips."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    H = 3
+    q, k, v = _inputs(1, M, H, seed=M + 7)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, M, q.device, head_dim=D)
+    for s0 in range(0, M, chunk):
+        Q.attn_chunk_step_split(q, k8, v8, s0, min(chunk, M - s0), st, split,
+                                k_offset_bytes=s0 * Q.row_bytes(D))
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want, *_ = oracle_out(q, k, v)
+    compare(out.cpu().numpy(), want, f"d128 causal split M{M} chunk{chunk} split{split}")
+
+
+def test_d128_static_split_matches_workspace_split(lib):
+    """The allocation-free split at head_dim 128 runs the same kernels on the
+    same inputs as the split with a caller workspace: identical state."""
+    import ctypes
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    M, H = 5000, 4
+    q, k, v = _inputs(1, M, H, seed=77, n_q=64)
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    a = Q.State(1, H, 64, q.device, head_dim=D)
+    b = Q.State(1, H, 64, q.device, head_dim=D)
+    Q.attn_chunk_step_split(q, k8, v8, 0, M, a, 1024, q_pos0=M, causal=False)
+    rc = lib.attn_chunk_step_split_static(
+        ctypes.c_void_p(q.data_ptr()), M, ctypes.c_void_p(k8.data_ptr()), ctypes.c_void_p(v8.data_ptr()),
+        k8.shape[-1], 0, M, ctypes.c_void_p(b.m.data_ptr()), ctypes.c_void_p(b.l.data_ptr()),
+        ctypes.c_void_p(b.o.data_ptr()), 1, H, 64, D, 1.0 / np.sqrt(D), 0, 1024,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == Q.Q8A_OK
+    torch.cuda.synchronize()
+    assert_device_clean()
+    assert torch.equal(a.m, b.m) and torch.equal(a.l, b.l) and torch.equal(a.o, b.o)
