@@ -119,3 +119,31 @@ def test_graph_create_reports_a_failing_call_and_leaves_no_capture(lib):
     assert_device_clean()
     _same(g, _eager(q, k, v, 128), M, 64)
     g.close()
+
+
+def test_graph_as_the_first_call_of_a_process(lib):
+    """A process whose first library call is the captured prefill (so the
+    kernels' one-time launch set-up happens while the graph is being recorded)
+    gets the same bits as the calls made one by one, at both head sizes."""
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    code = r"""
+import torch
+from chunked_prefill_attention_gb300 import q8attn as Q
+from tests.parity import seeded
+for D, chunk in ((64, 128), (128, 256)):
+    B, M, H = 1, 600, 2
+    q = seeded((B, M, H, D), 11 + D, "cuda", torch.float16)
+    k = seeded((B, M, H, D), 12 + D, "cuda")
+    v = seeded((B, M, H, D), 13 + D, "cuda")
+    g = Q.PrefillGraph(q, k, v, chunk)
+    g.launch()
+    torch.cuda.synchronize()
+    ref, *_ = Q.prefill_attention(q, k, v, chunk)
+    assert torch.equal(g.out, ref), D
+    g.close()
+print("ok")
+"""
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
