@@ -118,6 +118,7 @@ def test_quantiser_mutant_is_caught(name, old, new):
     assert not ok, f"planted mistake not caught: {name}"
 
 
+@pytest.mark.filterwarnings("ignore:invalid value encountered:RuntimeWarning")   # a mutant may produce NaN
 @pytest.mark.parametrize("name,old,new", ATTN_MUTANTS, ids=[m[0] for m in ATTN_MUTANTS])
 def test_attention_mutant_is_caught(name, old, new):
     try:
