@@ -342,13 +342,20 @@ int attn_chunk_step_gqa(const void* q, int64_t q_pos0, const void* k_q8, const v
   return ok();
 }
 
-int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
-                          int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
-                          float* m, float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
-                          int32_t head_dim, float scale, int32_t causal, int64_t split_keys,
-                          float* workspace, int64_t workspace_floats, void* stream) {
-  q8a::NvtxRange nvtx_range("attn_chunk_step_split");
-  const char* fn = "attn_chunk_step_split";
+}  // extern "C"
+
+namespace {
+
+// The split step behind attn_chunk_step_split (kv_heads = heads) and
+// attn_chunk_step_split_gqa.
+int split_step(const char* fn, const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+               int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m, float* l,
+               float* o, int64_t batch, int32_t heads, int32_t kv_heads, int64_t n_q, int32_t head_dim,
+               float scale, int32_t causal, int64_t split_keys, float* workspace,
+               int64_t workspace_floats, void* stream) {
+  if (kv_heads <= 0 || heads <= 0 || heads % kv_heads != 0)
+    return fail(Q8A_ERR_INVALID_ARG, "%s: heads (%d) must be a positive multiple of kv_heads (%d)",
+                fn, (int)heads, (int)kv_heads);
   if (head_dim != 64 && head_dim != 128)
     return fail(Q8A_ERR_UNSUPPORTED, "%s: head_dim must be 64 or 128 (got %d)", fn, head_dim);
   if (split_keys <= 0 || split_keys % 128 != 0)
@@ -382,12 +389,40 @@ int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const
   a.part_o = workspace;
   a.part_m = workspace + n_splits * rows * head_dim;
   a.part_l = a.part_m + n_splits * rows;
+  a.kv_heads = kv_heads;
   a.inject = g_inject.exchange(0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, st) : q8a::launch_chunk_step(qmap, a, st);
   if (e == cudaSuccess) e = q8a::launch_split_merge(a, st);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_chunk_step_split(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                          int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                          float* m, float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
+                          int32_t head_dim, float scale, int32_t causal, int64_t split_keys,
+                          float* workspace, int64_t workspace_floats, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_chunk_step_split");
+  return split_step("attn_chunk_step_split", q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start, kv_len, m,
+                    l, o, batch, heads, heads, n_q, head_dim, scale, causal, split_keys, workspace,
+                    workspace_floats, stream);
+}
+
+int attn_chunk_step_split_gqa(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
+                              int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                              float* m, float* l, float* o, int64_t batch, int32_t heads,
+                              int32_t kv_heads, int64_t n_q, int32_t head_dim, float scale,
+                              int32_t causal, int64_t split_keys, float* workspace,
+                              int64_t workspace_floats, void* stream) {
+  q8a::NvtxRange nvtx_range("attn_chunk_step_split_gqa");
+  return split_step("attn_chunk_step_split_gqa", q, q_pos0, k_q8, v_q8, kv_plane_stride_bytes, kv_start,
+                    kv_len, m, l, o, batch, heads, kv_heads, n_q, head_dim, scale, causal, split_keys,
+                    workspace, workspace_floats, stream);
 }
 
 }  // extern "C"

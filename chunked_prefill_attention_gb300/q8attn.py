@@ -43,6 +43,8 @@ SIGNATURES = {
                                            _I32, _I32, _I64, _I32, _F, _I32, _P]),
     "attn_chunk_step_split": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
                                              _I32, _I64, _I32, _F, _I32, _I64, _P, _I64, _P]),
+    "attn_chunk_step_split_gqa": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64,
+                                                 _I32, _I32, _I64, _I32, _F, _I32, _I64, _P, _I64, _P]),
     "q8a_split_workspace_floats": (_I64, [_I64, _I32, _I64, _I64, _I64]),
     "q8a_split_workspace_floats_for": (_I64, [_I64, _I32, _I64, _I64, _I64, _I32]),
     "attn_chunk_step_split_static": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P,
@@ -233,6 +235,28 @@ def attn_chunk_step_split(q, k8, v8, kv_start, kv_len, state, split_keys, worksp
                                      _ptr(state.m), _ptr(state.l), _ptr(state.o), B, H, n_q, D,
                                      scale, int(bool(causal)), split_keys, _ptr(workspace),
                                      workspace.numel(), _stream(q)))
+    return state
+
+
+def attn_chunk_step_split_gqa(q, k8, v8, kv_start, kv_len, state, split_keys, workspace=None, q_pos0=0,
+                              scale=None, causal=True, stride=None, k_offset_bytes=0):
+    """attn_chunk_step_split with k8, v8 holding H_kv planes per sequence
+    ([B, H_kv, stride]); query head h reads plane h // (H // H_kv)."""
+    B, n_q, H, D = q.shape
+    H_kv = k8.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stride is None:
+        stride = k8.shape[-1]
+    need = split_workspace_floats(B, H, n_q, kv_len, split_keys, D)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.float32, device=q.device)
+    kp = ctypes.c_void_p(k8.data_ptr() + k_offset_bytes)
+    vp = ctypes.c_void_p(v8.data_ptr() + k_offset_bytes)
+    _check(load().attn_chunk_step_split_gqa(_ptr(q), q_pos0, kp, vp, stride, kv_start, kv_len,
+                                            _ptr(state.m), _ptr(state.l), _ptr(state.o), B, H, H_kv, n_q, D,
+                                            scale, int(bool(causal)), split_keys, _ptr(workspace),
+                                            workspace.numel(), _stream(q)))
     return state
 
 

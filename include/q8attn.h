@@ -58,7 +58,8 @@ extern "C" {
  * pipelined call streams K and V through two chunk slots (kv_slots).  4:
  * head_dim 128 and q8a_plane_stride_bytes_for.  5: the captured prefill
  * (q8a_prefill_graph_*).  6: attn_prefill_pipelined and the split calls at
- * head_dim 128, q8a_prefill_slot_floats_for and q8a_split_workspace_floats_for. */
+ * head_dim 128, q8a_prefill_slot_floats_for, q8a_split_workspace_floats_for and
+ * attn_chunk_step_split_gqa. */
 #define Q8A_ABI_VERSION 6u
 
 enum {
@@ -209,6 +210,22 @@ int attn_chunk_step_split(const void *q, int64_t q_pos0, const void *k_q8, const
                           int64_t n_q, int32_t head_dim, float scale, int32_t causal,
                           int64_t split_keys, float *workspace, int64_t workspace_floats,
                           void *stream);
+
+/*
+ * attn_chunk_step_split_gqa -- attn_chunk_step_split for grouped-query
+ * attention: `heads` query heads on `kv_heads` K/V planes, query head h
+ * reading plane h / (heads / kv_heads), as for attn_chunk_step_gqa (burst
+ * verification of a model whose KV cache has fewer heads than its queries).
+ * The workspace is sized by the query heads (q8a_split_workspace_floats_for
+ * with `heads`).  Errors: as attn_chunk_step_split; Q8A_ERR_INVALID_ARG also
+ * when kv_heads <= 0 or heads is not a multiple of kv_heads.
+ */
+int attn_chunk_step_split_gqa(const void *q, int64_t q_pos0, const void *k_q8, const void *v_q8,
+                              int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len,
+                              float *m, float *l, float *o, int64_t batch, int32_t heads,
+                              int32_t kv_heads, int64_t n_q, int32_t head_dim, float scale,
+                              int32_t causal, int64_t split_keys, float *workspace,
+                              int64_t workspace_floats, void *stream);
 
 /* Floats of workspace attn_chunk_step_split needs at head_dim 64:
  * ceil(kv_len / split_keys) * batch * heads * n_q * 66; -1 for invalid sizes. */

@@ -70,3 +70,41 @@ def test_gqa_with_equal_head_counts_is_the_plain_step(lib):
     Q.attn_chunk_step_gqa(q, k8, v8, 0, M, b)
     assert_device_clean()
     assert torch.equal(a.m, b.m) and torch.equal(a.l, b.l) and torch.equal(a.o, b.o)
+
+
+@pytest.mark.parametrize("D,M,H,H_kv,split", [(64, 20000, 8, 2, 2048), (128, 5000, 6, 3, 1024),
+                                              (64, 3000, 4, 1, 384)])
+def test_gqa_split_burst(lib, D, M, H, H_kv, split):
+    """Burst verification for a grouped-query model: 64 candidates after the
+    context, the keys folded in parallel ranges over the shared K/V planes."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    from oracle import runner
+    from tests.parity import gpu_bytes
+    q = seeded((1, 64, H, D), M + D, "cuda", torch.float16)
+    k = seeded((1, M, H_kv, D), M + D + 1, "cuda")
+    v = seeded((1, M, H_kv, D), M + D + 2, "cuda")
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, 64, q.device, head_dim=D)
+    Q.attn_chunk_step_split_gqa(q, k8, v8, 0, M, st, split, q_pos0=M, causal=False)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    want = runner.attention(q.cpu().numpy(), gpu_bytes(k8, M, D), gpu_bytes(v8, M, D), 1.0 / np.sqrt(D),
+                            causal=False, q_pos0=M)
+    compare(out.cpu().numpy(), want, f"gqa split burst D{D} H{H}/{H_kv}")
+
+
+def test_gqa_split_causal_matches_unsplit(lib):
+    """Causal chunks folded with the grouped-query split and without it agree
+    within the parity tolerance, and the split output matches the oracle."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    M, H, H_kv, chunk = 1100, 6, 2, 512
+    q = seeded((1, M, H, 64), 95, "cuda", torch.float16)
+    k = seeded((1, M, H_kv, 64), 96, "cuda")
+    v = seeded((1, M, H_kv, 64), 97, "cuda")
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, M, q.device)
+    for s0 in range(0, M, chunk):
+        Q.attn_chunk_step_split_gqa(q, k8, v8, s0, min(chunk, M - s0), st, 256, k_offset_bytes=s0 * 68)
+    out = Q.attn_finalize(st)
+    assert_device_clean()
+    compare(out.cpu().numpy(), _oracle(q, k8, v8, M), "gqa causal split")
