@@ -524,15 +524,23 @@ def run_burst(args):
     torch.cuda.empty_cache()
     st = Q.State(1, H, b.queries, dev, init=False)
     out = torch.empty((1, b.queries, H, b.head_dim), dtype=torch.float16, device=dev)
-    split = b.split_keys or Q.split_keys_for(H, M, torch.cuda.get_device_properties(dev).multi_processor_count)
+    # CTAs per key range: one per (b, h), or with grouped-query packing one per
+    # (b, K/V head) and 256 (candidate, head) rows
+    group = H // b.kv_h
+    packed = group >= 2 and 128 % group == 0 and b.head_dim == 64
+    ctas = b.kv_h * -(-b.queries * group // 256) if packed else H
+    split = b.split_keys or Q.split_keys_for(ctas, M, torch.cuda.get_device_properties(dev).multi_processor_count)
     ws = torch.empty(Q.split_workspace_floats(1, H, b.queries, M, split), dtype=torch.float32,
                      device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         Q.attn_state_init(st)
-        Q.attn_chunk_step_split(q, k8, v8, 0, M, st, split, workspace=ws, q_pos0=M,
-                                causal=False)
+        if b.kv_h != H:
+            Q.attn_chunk_step_split_gqa(q, k8, v8, 0, M, st, split, workspace=ws, q_pos0=M, causal=False)
+        else:
+            Q.attn_chunk_step_split(q, k8, v8, 0, M, st, split, workspace=ws, q_pos0=M,
+                                    causal=False)
         Q.attn_finalize(st, out)
 
     for _ in range(max(args.warmup, 0)):
@@ -585,13 +593,23 @@ def run_burst(args):
     config = {"workload": b.describe(), "batch": 1, "tokens": M, "queries": b.queries, "heads": H,
               "head_dim": b.head_dim, "split_keys": split, "key_ranges": -(-M // split), "replicas": world,
               "l2": "Q8_0 KV %.2f GB, larger than L2" % (b.kv_bytes / 1e9)}
+    tflops = world * b.flops / (ms * 1e-3) / 1e12
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    hbm_roof = {"bound": "hbm", "kernel": "attn_chunk_step_split + merge", "achieved": gbs,
+                "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_kind": f"HBM copy bandwidth, {peak_src}",
+                "algorithmic": "2*H_kv*M*(D/32*34) bytes of Q8_0 K and V per step", "traffic": None}
+    tensor_roof = {"bound": "tensor", "kernel": "attn_chunk_step_split + merge", "achieved": tflops,
+                   "peak": peak_t, "unit": "TFLOP/s", "frac": tflops / peak_t,
+                   "peak_kind": f"dense bf16/fp16 {peak_src} sustained",
+                   "algorithmic": "4*D flops per (candidate, context key) pair and query head", "traffic": None}
+    # the binding resource: a grouped-query burst reads each K/V plane once for
+    # several query heads, so it can be bound by the tensor work instead
     extra = {
         "candidate_tokens_per_s": world * b.queries / (ms * 1e-3),
-        "tflops": world * b.flops / (ms * 1e-3) / 1e12,
-        "roofline": {"bound": "hbm", "kernel": "attn_chunk_step_split + merge", "achieved": gbs,
-                     "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                     "peak_kind": f"HBM copy bandwidth, {peak_src}",
-                     "algorithmic": "2*H*M*68 bytes of Q8_0 K and V per step", "traffic": None},
+        "tflops": tflops,
+        "roofline": hbm_roof if hbm_roof["frac"] >= tensor_roof["frac"] else tensor_roof,
+        "roofline_other": tensor_roof if hbm_roof["frac"] >= tensor_roof["frac"] else hbm_roof,
         "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * 4, "cpu_baseline": None,
     }
     rec = make_record(value=gbs, n_gpus=world, steps=args.steps, warmup=args.warmup,

@@ -346,6 +346,26 @@ int attn_chunk_step_gqa(const void* q, int64_t q_pos0, const void* k_q8, const v
 
 namespace {
 
+// Q as the packed A operand of grouped-query bursts: a 3-D view {64 channels,
+// heads, batch * n_q rows} of the fp16 [B][n_q][H][64] tensor with a box of
+// {64, group, 128 / group}, so one box is 128 rows ordered (query row, head of
+// the group), 128-byte swizzled like the plain query tile.
+int encode_q_packed(const char* fn, const void* q, int64_t batch, int32_t heads, int64_t n_q,
+                    int32_t group, CUtensorMap* qmap) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
+  std::memset(qmap, 0, sizeof(*qmap));
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch * n_q)};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(heads) * 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult cr = enc(qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(Q8A_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", fn, (int)cr);
+  return Q8A_OK;
+}
+
 // The split step behind attn_chunk_step_split (kv_heads = heads) and
 // attn_chunk_step_split_gqa.
 int split_step(const char* fn, const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
@@ -390,10 +410,23 @@ int split_step(const char* fn, const void* q, int64_t q_pos0, const void* k_q8, 
   a.part_m = workspace + n_splits * rows * head_dim;
   a.part_l = a.part_m + n_splits * rows;
   a.kv_heads = kv_heads;
+  q8a::ChunkArgs merge = a;   // the merge walks every (batch, query head, row)
+  // Few query rows over grouped K/V heads (a burst): the tiles take (query row,
+  // query head) pairs of one K/V group, so each dequantised key tile serves
+  // all the group's heads instead of one.
+  const int32_t group = heads / kv_heads;
+  if (head_dim == 64 && !causal && group >= 2 && 128 % group == 0) {
+    if (int rc = encode_q_packed(fn, q, batch, heads, n_q, group, &qmap)) return rc;
+    a.pack = group;
+    a.bh = static_cast<int32_t>(batch * kv_heads);
+    a.tile0 = 0;
+    a.n_qtiles = static_cast<int32_t>((n_q * group + 127) / 128);
+    a.pair = 0;
+  }
   a.inject = g_inject.exchange(0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, st) : q8a::launch_chunk_step(qmap, a, st);
-  if (e == cudaSuccess) e = q8a::launch_split_merge(a, st);
+  if (e == cudaSuccess) e = q8a::launch_split_merge(merge, st);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }

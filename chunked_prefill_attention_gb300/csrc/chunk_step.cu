@@ -248,7 +248,9 @@ __device__ __forceinline__ Range make_range(const ChunkArgs& a) {
   r.fresh = false;
   if (a.split_keys > 0) {
     const int64_t off = static_cast<int64_t>(blockIdx.y) * a.split_keys;
-    const int64_t rows = static_cast<int64_t>(a.bh) * a.n_q;
+    // state rows (batch, query head, query row); with packing bh counts K/V heads
+    const int64_t rows = a.pack ? static_cast<int64_t>(a.bh / a.kv_heads) * a.heads * a.n_q
+                                : static_cast<int64_t>(a.bh) * a.n_q;
     r.kv_len = i64min(a.split_keys, a.kv_len - off);
     r.kv_start = a.kv_start + off;
     r.k8 = a.k8 + off * kRowBytes;
@@ -288,8 +290,10 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   const int64_t idx = blockIdx.x;
   u.bh = idx / a.n_qtiles;   // n_qtiles counts 256-row units here
   const int64_t qu = a.n_qtiles - 1 - (idx % a.n_qtiles);   // heavy units first
-  u.b = u.bh / a.heads;
-  u.h = u.bh % a.heads;
+  // u.h: the query head, or with packing the K/V head of the unit
+  const int32_t nh = a.pack ? a.kv_heads : a.heads;
+  u.b = u.bh / nh;
+  u.h = u.bh % nh;
   u.r0 = static_cast<int64_t>(a.tile0) * BM + qu * (NQT * BM);
   u.T_all = 0;
   if (a.pair) {
@@ -299,14 +303,16 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
     u.T_all = tiles;
     return u;
   }
+  const int64_t n_rows = a.pack ? a.n_q * a.pack : a.n_q;   // rows of the tile space
 #pragma unroll
   for (int x = 0; x < NQT; ++x) {
     const int64_t rx = u.r0 + x * BM;
     u.T[x] = 0;
-    if (rx < a.n_q) {
-      const int64_t r_last = i64min(rx + BM - 1, a.n_q - 1);
+    if (rx < n_rows) {
+      const int64_t r_last = i64min(rx + BM - 1, n_rows - 1);
+      const int64_t last_pos = a.q_pos0 + (a.pack ? r_last / a.pack : r_last);
       int64_t n_vis = kr.kv_len;
-      if (a.causal) n_vis = i64min(n_vis, a.q_pos0 + r_last - kr.kv_start + 1);
+      if (a.causal) n_vis = i64min(n_vis, last_pos - kr.kv_start + 1);
       u.T[x] = n_vis > 0 ? static_cast<int>((n_vis + BN - 1) / BN) : 0;
     }
     u.T_all = max(u.T_all, u.T[x]);
@@ -332,10 +338,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
       mbar_arrive_expect_tx(bar(B_QFULL), nq * BM * 128);
 #pragma unroll
       for (int x = 0; x < NQT; ++x)
-        if (u.T[x] > 0)
-          tma_load_3d(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL),
-                      static_cast<int32_t>(u.h * kHeadDim), static_cast<int32_t>(u.r0 + tile_row0(a, x)),
-                      static_cast<int32_t>(u.b));
+        if (u.T[x] > 0) {
+          if (a.pack)   // box {64 channels, pack heads, 128 / pack query rows}
+            tma_load_3d(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL), 0,
+                        static_cast<int32_t>(u.h * a.pack),
+                        static_cast<int32_t>(u.b * a.n_q + (u.r0 + tile_row0(a, x)) / a.pack));
+          else
+            tma_load_3d(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL),
+                        static_cast<int32_t>(u.h * kHeadDim), static_cast<int32_t>(u.r0 + tile_row0(a, x)),
+                        static_cast<int32_t>(u.b));
+        }
     }
   }
   int last_bulk[NR];
@@ -344,7 +356,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
 
   // K/V plane of this query head (grouped-query attention: heads / kv_heads
   // query heads share one plane)
-  const int64_t kv_plane = u.b * a.kv_heads + u.h / (a.heads / a.kv_heads);
+  const int64_t kv_plane = a.pack ? u.b * a.kv_heads + u.h : u.b * a.kv_heads + u.h / (a.heads / a.kv_heads);
   const uint8_t* kp = kr.k8 + kv_plane * a.plane_stride;
   const uint8_t* vp = kr.v8 + kv_plane * a.plane_stride;
   for (int t = 0; t < u.T_all; ++t) {
@@ -653,10 +665,13 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
   const int T = u.T[x];
   if (T == 0) return;
 
-  const int64_t rg = u.r0 + tile_row0(a, x) + row;
+  // this thread's row of the tile space; with packing a (query row, query
+  // head) pair of the unit's K/V group
+  const int64_t pr = u.r0 + tile_row0(a, x) + row;
+  const int64_t rg = a.pack ? pr / a.pack : pr;   // query row
   const int64_t pos = a.q_pos0 + rg;
   const bool active = rg < a.n_q && (!a.causal || pos >= kr.kv_start);
-  const int64_t sidx = u.bh * a.n_q + rg;
+  const int64_t sidx = a.pack ? (u.b * a.heads + u.h * a.pack + pr % a.pack) * a.n_q + rg : u.bh * a.n_q + rg;
   const uint32_t t_s = tmem + lane_off + T_S + 128u * x;
   const uint32_t t_o = tmem + lane_off + T_O + 128u * x;
 
@@ -695,7 +710,8 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
   }
 
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
-  const int64_t q_first = a.q_pos0 + u.r0 + tile_row0(a, x);   // position of the tile's first row
+  // position of the tile's first row
+  const int64_t q_first = a.q_pos0 + (a.pack ? (u.r0 + tile_row0(a, x)) / a.pack : u.r0 + tile_row0(a, x));
   bool ok = true;
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {

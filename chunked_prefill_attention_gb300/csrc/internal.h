@@ -98,6 +98,11 @@ struct ChunkArgs {
   int32_t head_dim;       // 64 or 128
   int32_t pair;           // 1: one query tile, no causal mask -- the CTA's two softmax
                           // pipelines share the rows and split the key tiles (even / odd)
+  int32_t pack;           // grouped-query bursts (head_dim 64, no causal mask): a tile's
+                          // rows are (query row, query head) pairs of the `pack` query
+                          // heads that share one K/V plane, row = query row * pack +
+                          // head in the group; bh then counts (batch, K/V head) units
+                          // and n_qtiles the 128-row tiles of n_q * pack rows; 0 = off
   uint64_t timeout_ns;    // budget of every device-side wait
   // Split form (split_keys > 0): block row y of the grid folds keys
   // [y*split_keys, min((y+1)*split_keys, kv_len)) of the chunk into an empty

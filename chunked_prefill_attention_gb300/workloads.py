@@ -22,7 +22,7 @@ The pages measure no public dataset; these draws stand in for the activations
 of a prefill pass.  Inputs are drawn with a torch generator on the device they
 are created on, in the fixed order Q, then K, then V.
 
-Mode B (speculative burst verification) has one workload of its own:
+Mode B (speculative burst verification) has workloads of its own:
 
   burst_m1m  64 candidate queries at positions M .. M+63 against an
              M = 1,048,576-token context, 32 heads x 64, rectangular
@@ -30,6 +30,8 @@ Mode B (speculative burst verification) has one workload of its own:
              the context's keys are folded in parallel key ranges whose
              count makes the launch a whole number of waves on the device
              (q8attn.split_keys_for: 19 ranges of 55,296 keys on 152 SMs).
+  burst_m1m_gqa8  the same with 32 query heads on 8 K/V heads (seed 7):
+             grouped-query attention, an extension beyond the pages.
 """
 
 from dataclasses import dataclass
@@ -93,11 +95,16 @@ class Burst:
     seed: int
     heads: int = HEADS
     head_dim: int = HEAD_DIM
+    kv_heads: int = 0   # K/V heads (grouped-query attention); 0: as many as query heads
+
+    @property
+    def kv_h(self):
+        return self.kv_heads or self.heads
 
     @property
     def kv_bytes(self):
-        """Q8_0 K and V of the context: 2 * H * M * 68 bytes."""
-        return 2 * self.heads * self.context * 68
+        """Q8_0 K and V of the context: 2 * H_kv * M * (D / 32 * 34) bytes."""
+        return 2 * self.kv_h * self.context * (self.head_dim // 32 * 34)
 
     @property
     def flops(self):
@@ -106,23 +113,25 @@ class Burst:
 
     def describe(self):
         return (f"{self.name}: {self.queries} candidate queries after a {self.context}-token context, "
-                f"H={self.heads} D={self.head_dim}, rectangular mask, key ranges "
+                f"H={self.heads}" + (f" on {self.kv_h} K/V heads" if self.kv_h != self.heads else "")
+                + f" D={self.head_dim}, rectangular mask, key ranges "
                 + (f"of {self.split_keys}" if self.split_keys else "sized to whole waves")
                 + f", seed {self.seed}")
 
 
-BURSTS = {b.name: b for b in [Burst("burst_m1m", 1048576, 64, 0, 5)]}
+BURSTS = {b.name: b for b in [Burst("burst_m1m", 1048576, 64, 0, 5),
+                              Burst("burst_m1m_gqa8", 1048576, 64, 0, 7, kv_heads=8)]}
 
 
 def make_burst_inputs(b, device="cpu", context=None):
-    """Draw (Q fp16 [1, queries, H, D], K fp32 [1, M, H, D], V fp32), in that order."""
+    """Draw (Q fp16 [1, queries, H, D], K fp32 [1, M, H_kv, D], V fp32), in that order."""
     M = b.context if context is None else context
     g = torch.Generator(device=device)
     g.manual_seed(b.seed)
     q = torch.randn((1, b.queries, b.heads, b.head_dim), generator=g, device=device,
                     dtype=torch.float32).to(torch.float16)
-    k = torch.randn((1, M, b.heads, b.head_dim), generator=g, device=device, dtype=torch.float32)
-    v = torch.randn((1, M, b.heads, b.head_dim), generator=g, device=device, dtype=torch.float32)
+    k = torch.randn((1, M, b.kv_h, b.head_dim), generator=g, device=device, dtype=torch.float32)
+    v = torch.randn((1, M, b.kv_h, b.head_dim), generator=g, device=device, dtype=torch.float32)
     return q, k, v
 
 

@@ -72,19 +72,25 @@ def test_gqa_with_equal_head_counts_is_the_plain_step(lib):
     assert torch.equal(a.m, b.m) and torch.equal(a.l, b.l) and torch.equal(a.o, b.o)
 
 
-@pytest.mark.parametrize("D,M,H,H_kv,split", [(64, 20000, 8, 2, 2048), (128, 5000, 6, 3, 1024),
-                                              (64, 3000, 4, 1, 384)])
-def test_gqa_split_burst(lib, D, M, H, H_kv, split):
-    """Burst verification for a grouped-query model: 64 candidates after the
-    context, the keys folded in parallel ranges over the shared K/V planes."""
+@pytest.mark.parametrize("D,M,H,H_kv,split,n_q,B", [(64, 20000, 8, 2, 2048, 64, 1), (128, 5000, 6, 3, 1024, 64, 1),
+                                                     (64, 3000, 4, 1, 384, 64, 1), (64, 4000, 16, 2, 512, 70, 2),
+                                                     (64, 2500, 8, 4, 1024, 64, 1), (64, 1800, 8, 1, 256, 33, 1),
+                                                     (64, 1000, 6, 2, 128, 64, 1)])
+def test_gqa_split_burst(lib, D, M, H, H_kv, split, n_q, B):
+    """Burst verification for a grouped-query model: candidates after the
+    context, the keys folded in parallel ranges over the shared K/V planes.  At
+    head_dim 64 with a group of 2, 4 or 8 heads the tiles take (candidate,
+    head) pairs of one group (70 candidates x 8 heads: a ragged last tile whose
+    extra rows read the next sequence's queries and stay inactive; a group of
+    3 is not a divisor of 128 and keeps one head per tile)."""
     from chunked_prefill_attention_gb300 import q8attn as Q
     from oracle import runner
     from tests.parity import gpu_bytes
-    q = seeded((1, 64, H, D), M + D, "cuda", torch.float16)
-    k = seeded((1, M, H_kv, D), M + D + 1, "cuda")
-    v = seeded((1, M, H_kv, D), M + D + 2, "cuda")
+    q = seeded((B, n_q, H, D), M + D, "cuda", torch.float16)
+    k = seeded((B, M, H_kv, D), M + D + 1, "cuda")
+    v = seeded((B, M, H_kv, D), M + D + 2, "cuda")
     k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
-    st = Q.State(1, H, 64, q.device, head_dim=D)
+    st = Q.State(B, H, n_q, q.device, head_dim=D)
     Q.attn_chunk_step_split_gqa(q, k8, v8, 0, M, st, split, q_pos0=M, causal=False)
     out = Q.attn_finalize(st)
     assert_device_clean()

@@ -169,3 +169,35 @@ def test_burst_verification_bench_shape(lib):
         want = oracle_runner.attention(qn[:, :, h:h + 1], wk8, wv8, 0.125, causal=False, q_pos0=M)
         res = compare(out[:, :, h:h + 1], want, f"burst_m1m head {h}")
         print(f"\n[burst_m1m head {h}] max|err| {res[0]:.3e} (|out| {res[2]:.2f}), rel-L2 {res[1]:.3e}")
+
+
+def test_grouped_query_burst_bench_shape(lib):
+    """The grouped-query burst benchmark's case: 64 candidates of 32 query
+    heads on 8 K/V heads against a 1,048,576-token context, launched as the
+    benchmark does (packed tiles of (candidate, head) pairs, wave-sized key
+    ranges); the oracle checks the Q8_0 bytes of two K/V heads and the output
+    of three query heads."""
+    from chunked_prefill_attention_gb300 import q8attn as Q, workloads as W
+    from oracle import runner as oracle_runner
+    b = W.BURSTS["burst_m1m_gqa8"]
+    M, H, H_kv = b.context, b.heads, b.kv_h
+    g = H // H_kv
+    q, k, v = W.make_burst_inputs(b, device="cuda")
+    k8, v8 = Q.q8kv_quantize(k), Q.q8kv_quantize(v)
+    st = Q.State(1, H, b.queries, q.device)
+    ctas = H_kv * -(-b.queries * g // 256)
+    split = Q.split_keys_for(ctas, M, torch.cuda.get_device_properties(0).multi_processor_count)
+    Q.attn_chunk_step_split_gqa(q, k8, v8, 0, M, st, split, q_pos0=M, causal=False)
+    out = Q.attn_finalize(st).cpu().numpy()
+    assert_device_clean()
+    qn = q.cpu().numpy()
+    for h in [0, 13, 31]:
+        kvh = h // g
+        wk8 = oracle_runner.quantize_kv(k[:, :, kvh:kvh + 1].contiguous().cpu().numpy())
+        wv8 = oracle_runner.quantize_kv(v[:, :, kvh:kvh + 1].contiguous().cpu().numpy())
+        if h in (0, 31):
+            assert np.array_equal(k8[:, kvh:kvh + 1, :M * 68].reshape(1, 1, M, 68).cpu().numpy(), wk8)
+            assert np.array_equal(v8[:, kvh:kvh + 1, :M * 68].reshape(1, 1, M, 68).cpu().numpy(), wv8)
+        want = oracle_runner.attention(qn[:, :, h:h + 1], wk8, wv8, 0.125, causal=False, q_pos0=M)
+        res = compare(out[:, :, h:h + 1], want, f"burst_m1m_gqa8 head {h}")
+        print(f"\n[burst_m1m_gqa8 head {h}] max|err| {res[0]:.3e} (|out| {res[2]:.2f}), rel-L2 {res[1]:.3e}")
