@@ -224,6 +224,23 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, __half2& lo, __half2&
 }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// The order of a launch's CTAs over (b, h) units and query units.  The (b, h)
+// units are taken in groups of kHeadGroup; within a group the CTAs run the
+// heaviest query units first, the group's (b, h) fastest.  So the longest
+// CTAs of a group start together and the launch ends on the lightest ones (a
+// near-even finish across the SMs), while the K/V planes read at any one time
+// are those of one group, few enough to stay in L2 between the group's CTAs.
+// Every idx < units * n_bh gets a distinct (bh, qu).
+constexpr int64_t kHeadGroup = 8;
+__device__ __forceinline__ void cta_order(int64_t idx, int64_t units, int64_t n_bh, int64_t& bh, int64_t& qu) {
+  const int64_t full = n_bh / kHeadGroup;   // complete groups
+  const int64_t g = idx / (units * kHeadGroup);
+  const int64_t gs = g < full ? kHeadGroup : n_bh - full * kHeadGroup;   // heads in this group
+  const int64_t w = idx - g * units * kHeadGroup;
+  bh = g * kHeadGroup + w % gs;
+  qu = units - 1 - w / gs;
+}
+
 // The key range and state this CTA works on: the whole chunk and the state,
 // or, in the split form, one key range and its partial state.
 struct Range {
@@ -287,9 +304,9 @@ __device__ __forceinline__ int key_tile(const ChunkArgs& a, int x, int j) {
 
 __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
-  const int64_t idx = blockIdx.x;
-  u.bh = idx / a.n_qtiles;   // n_qtiles counts 256-row units here
-  const int64_t qu = a.n_qtiles - 1 - (idx % a.n_qtiles);   // heavy units first
+  int64_t bh, qu;   // n_qtiles counts 256-row units here
+  cta_order(blockIdx.x, a.n_qtiles, a.bh, bh, qu);
+  u.bh = bh;
   // u.h: the query head, or with packing the K/V head of the unit
   const int32_t nh = a.pack ? a.kv_heads : a.heads;
   u.b = u.bh / nh;
@@ -1022,9 +1039,9 @@ __device__ __forceinline__ Range make_range(const ChunkArgs& a) {
 
 __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
-  const int64_t idx = blockIdx.x;
-  u.bh = idx / a.n_qtiles;
-  const int64_t qt = a.n_qtiles - 1 - (idx % a.n_qtiles);   // heavy tiles first
+  int64_t bh, qt;
+  cta_order(blockIdx.x, a.n_qtiles, a.bh, bh, qt);
+  u.bh = bh;
   u.b = u.bh / a.heads;
   u.h = u.bh % a.heads;
   u.r0 = (static_cast<int64_t>(a.tile0) + qt) * BM;
@@ -1572,9 +1589,9 @@ struct Unit {
 __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
   Unit u;
   const int64_t units = (static_cast<int64_t>(a.n_qtiles) + 1) / 2;
-  const int64_t idx = blockIdx.x;
-  u.bh = idx / units;
-  const int64_t qu = units - 1 - (idx % units);   // heavy units first
+  int64_t bh, qu;
+  cta_order(blockIdx.x, units, a.bh, bh, qu);
+  u.bh = bh;
   u.b = u.bh / a.heads;
   u.h = u.bh % a.heads;
   u.r0 = (static_cast<int64_t>(a.tile0) + 2 * qu) * BM;

@@ -95,6 +95,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// --------------------------------------------------- L2 eviction priority --
+// A cache policy that marks the lines it touches as the first to leave L2.
+// Given to the loads of data a kernel reads once (the quantiser's fp32 input),
+// so that they do not push out lines that are read again soon: the Q8_0 rows
+// a quantise has just written for the chunk step that follows it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -64,12 +64,23 @@ __device__ __forceinline__ uint2 code_pair(float2 x, float2 nd2, float2 y2) {
   return make_uint2(__float_as_uint(u.x), __float_as_uint(u.y));
 }
 
-// 256-bit read-only load of eight consecutive floats (32-byte aligned).
-__device__ __forceinline__ void ldg256(const float* p, float* v) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+// 256-bit read-only load of eight consecutive floats (32-byte aligned).  The
+// input is read once, so its lines go first when L2 needs room (`policy` is
+// the evict-first policy); the Q8_0 rows written here stay for the chunk step
+// that reads them next.
+__device__ __forceinline__ void ldg256(const float* p, float* v, uint64_t policy) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
                  "=f"(v[6]), "=f"(v[7])
-               : "l"(p));
+               : "l"(p), "l"(policy));
+}
+// 128-bit read-only load with the same policy.
+__device__ __forceinline__ float4 ldg128(const float* p, uint64_t policy) {
+  float4 f;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+               : "l"(p), "l"(policy));
+  return f;
 }
 
 // kD: channels per head row (64 or 128: kD / 32 Q8_0 blocks, kD / 32 * 34
@@ -107,13 +118,14 @@ q8kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int
   float v[32];
   if (valid) {
     const float* src = x + (((b * n_tokens + t0 + tok) * heads + h0 + hh) * kD + 32 * bb);
+    const uint64_t pol = l2_evict_first_policy();
     if (kWide) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ldg256(src + 8 * i, v + 8 * i);
+      for (int i = 0; i < 4; ++i) ldg256(src + 8 * i, v + 8 * i, pol);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(src) + i);
+        const float4 f = ldg128(src + 4 * i, pol);
         v[4 * i] = f.x;
         v[4 * i + 1] = f.y;
         v[4 * i + 2] = f.z;
