@@ -239,6 +239,11 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
   a->causal = causal ? 1 : 0;
   a->pair = (!causal && n_qtiles == 1) ? 1 : 0;
   a->head_dim = head_dim;
+  {
+    const int64_t kv_head_bytes = 2 * kv_len * row_bytes(head_dim);   // one head's K and V of the chunk
+    const int64_t g = (int64_t{16} << 20) / kv_head_bytes;
+    a->head_group = static_cast<int32_t>(g < 1 ? 1 : (g > 8 ? 8 : g));
+  }
   a->timeout_ns = g_timeout_ns.load();
   return Q8A_OK;
 }

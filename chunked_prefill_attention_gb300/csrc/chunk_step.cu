@@ -16,14 +16,15 @@
 //              tile (TMEM lane i).  Per key tile it loads its whole 128-score S
 //              row from TMEM into registers, masks diagonal and tail tiles,
 //              takes the row max, forms beta = ex2(S*c - m*log2e) with packed
-//              fp32x2 arithmetic against the running max m (so the weight of
-//              the row's largest score is exactly 1), sums beta in fp32 and
-//              writes P = fp16(beta) over the first 64 columns of its S row, in
-//              two halves (keys 0-63, then 64-127) announced on separate
-//              barriers so that the first half of PV runs while the second
-//              half is computed.  A warp rescales its O rows in TMEM, before
-//              the first half is announced, only when the max of one of its
-//              rows moved.
+//              fp32x2 arithmetic against the reference m, sums beta in fp32
+//              (with the tile max's weight as fp16 rounds it) and writes
+//              P = fp16(beta) over the first 64 columns of its S row, in two
+//              halves (keys 0-63, then 64-127) announced on separate barriers
+//              so that the first half of PV runs while the second half is
+//              computed.  The reference m moves to the tile max only when that
+//              exceeds it by more than 8 ln 2 (weights stay below 2^8); a warp
+//              rescales its O rows in TMEM, before the first half is
+//              announced, only when the reference of one of its rows moved.
 //   WG2        dequant, one thread per key row.  K = d*q and V = d*q are each
 //              split exactly into an fp16 high part fp16(d*q) and an fp16
 //              residual fp16(d*q - high) (half2 multiply / fma on codes
@@ -118,6 +119,19 @@ constexpr uint32_t T_S = 0;      // + 128 * tile
 constexpr uint32_t T_O = 256;    // + 128 * tile; high half at +0, residual half at +64
 
 constexpr float kLog2e = 1.4426950408889634f;
+// The softmax reference m moves only when a tile's max exceeds it by more than
+// 8 ln 2, so the weights stay below 2^8 and O is rescaled only then.
+constexpr float kLazyNat = 5.545177444479562f;
+
+// l sums the fp32 weights beta, P holds them rounded to fp16.  For the tile's
+// largest score (raw score mx) this returns fp16(beta) - beta, which l adds, so
+// that a row dominated by one key divides that key's term by exactly the
+// weight P gave it.  0 when every key of the tile is masked.
+__device__ __forceinline__ float p_max_correction(float mx, float scale_log2, float mlog) {
+  if (mx == -INFINITY) return 0.0f;
+  const float bm = ex2_approx(fmaf(mx, scale_log2, -mlog));   // as the P loop forms it
+  return __half2float(__float2half_rn(bm)) - bm;
+}
 
 // role ids recorded in the status word when a wait runs out
 enum : uint32_t { R_SOFTMAX = 1, R_DEQUANT = 2, R_PRODUCER = 3, R_MMA = 4, R_DRAIN = 5 };
@@ -225,19 +239,19 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, __half2& lo, __half2&
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // The order of a launch's CTAs over (b, h) units and query units.  The (b, h)
-// units are taken in groups of kHeadGroup; within a group the CTAs run the
-// heaviest query units first, the group's (b, h) fastest.  So the longest
-// CTAs of a group start together and the launch ends on the lightest ones (a
-// near-even finish across the SMs), while the K/V planes read at any one time
-// are those of one group, few enough to stay in L2 between the group's CTAs.
-// Every idx < units * n_bh gets a distinct (bh, qu).
-constexpr int64_t kHeadGroup = 8;
-__device__ __forceinline__ void cta_order(int64_t idx, int64_t units, int64_t n_bh, int64_t& bh, int64_t& qu) {
-  const int64_t full = n_bh / kHeadGroup;   // complete groups
-  const int64_t g = idx / (units * kHeadGroup);
-  const int64_t gs = g < full ? kHeadGroup : n_bh - full * kHeadGroup;   // heads in this group
-  const int64_t w = idx - g * units * kHeadGroup;
-  bh = g * kHeadGroup + w % gs;
+// units are taken in groups of `group` (ChunkArgs::head_group); within a group
+// the CTAs run the heaviest query units first, the group's (b, h) fastest.  So
+// the longest CTAs of a group start together and the launch ends on the
+// lightest ones (a near-even finish across the SMs), while the K/V planes read
+// at any one time are those of one group, few enough to stay in L2 between the
+// group's CTAs.  Every idx < units * n_bh gets a distinct (bh, qu).
+__device__ __forceinline__ void cta_order(int64_t idx, int64_t units, int64_t n_bh, int64_t group, int64_t& bh,
+                                          int64_t& qu) {
+  const int64_t full = n_bh / group;   // complete groups
+  const int64_t g = idx / (units * group);
+  const int64_t gs = g < full ? group : n_bh - full * group;   // heads in this group
+  const int64_t w = idx - g * units * group;
+  bh = g * group + w % gs;
   qu = units - 1 - w / gs;
 }
 
@@ -305,7 +319,7 @@ __device__ __forceinline__ int key_tile(const ChunkArgs& a, int x, int j) {
 __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
   int64_t bh, qu;   // n_qtiles counts 256-row units here
-  cta_order(blockIdx.x, a.n_qtiles, a.bh, bh, qu);
+  cta_order(blockIdx.x, a.n_qtiles, a.bh, a.head_group, bh, qu);
   u.bh = bh;
   // u.h: the query head, or with packing the K/V head of the unit
   const int32_t nh = a.pack ? a.kv_heads : a.heads;
@@ -631,8 +645,8 @@ __device__ __forceinline__ void mma_role(const ChunkArgs& a, const Unit& u, uint
 // Paired mode: fold tile B's final state (m_b, l_b; O at TMEM address t_ob)
 // into tile A's (m_a, l_a; O at t_oa) and write the result -- the chunk
 // recurrence applied to two partial states over disjoint keys.  The weight of
-// the state holding the larger max is exactly 1.  O is the sum of each tile's
-// high and residual halves.
+// the state holding the larger reference m is exactly 1.  O is the sum of each
+// tile's high and residual halves.
 __device__ __forceinline__ void merge_pair_out(const Range& kr, int64_t sidx, bool active,
                                                float m_a, float l_a, float m_b, float l_b,
                                                uint32_t t_oa, uint32_t t_ob) {
@@ -766,7 +780,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
     const float mx = fmaxf(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], max3(pm[5], pm[6], pm[7])));
     const float t_nat = mx * a.scale;   // -inf when every key of the tile is masked
     float alpha = 1.0f;
-    const bool resc = t_nat > m_run;      // the running max moves
+    const bool resc = t_nat > m_run + kLazyNat;   // the reference moves
     if (resc) {
       alpha = (m_run == -INFINITY) ? 0.0f : ex2_approx((m_run - t_nat) * kLog2e);
       m_run = t_nat;
@@ -827,7 +841,8 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
     tc_fence_before();
     mbar_arrive(bar(B_PFULL + 2 * x + 1));
     const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-    l_run = fmaf(l_run, alpha, r.x + r.y);   // same ops per tile with or without chunking
+    // same ops per tile with or without chunking
+    l_run = fmaf(l_run, alpha, (r.x + r.y) + p_max_correction(mx, a.scale_log2, mlog));
   }
   float4* xch = reinterpret_cast<float4*>(smem + OFF_XCH) + row;
   if (pair_merge && x == 1) {
@@ -1040,7 +1055,7 @@ __device__ __forceinline__ Range make_range(const ChunkArgs& a) {
 __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
   Unit u;
   int64_t bh, qt;
-  cta_order(blockIdx.x, a.n_qtiles, a.bh, bh, qt);
+  cta_order(blockIdx.x, a.n_qtiles, a.bh, a.head_group, bh, qt);
   u.bh = bh;
   u.b = u.bh / a.heads;
   u.h = u.bh % a.heads;
@@ -1374,7 +1389,7 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Range& kr, con
     const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
     const float t_nat = mx * a.scale;
     float alpha = 1.0f;
-    const bool resc = t_nat > m_run;
+    const bool resc = t_nat > m_run + kLazyNat;   // the reference moves
     if (resc) {
       alpha = (m_run == -INFINITY) ? 0.0f : ex2_approx((m_run - t_nat) * kLog2e);
       m_run = t_nat;
@@ -1400,7 +1415,7 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Range& kr, con
     tc_fence_before();
     mbar_arrive(bar(B_PFULL + x));
     const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-    l_run = fmaf(l_run, alpha, r.x + r.y);
+    l_run = fmaf(l_run, alpha, (r.x + r.y) + p_max_correction(mx, a.scale_log2, mlog));
   }
   float4* xch = reinterpret_cast<float4*>(smem + OFF_XCH) + row;
   if (pair_merge && x == 1) {
@@ -1423,7 +1438,7 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Range& kr, con
     l_b = pb.y;
   }
   // the chunk recurrence over the two partial states (B's weight is 0 when
-  // it holds no key); the weight of the larger max is exactly 1
+  // it holds no key); the weight of the larger reference is exactly 1
   const float m = fmaxf(m_run, m_b);
   const float wa = (m_run == m) ? 1.0f : (m_run == -INFINITY ? 0.0f : ex2_approx((m_run - m) * kLog2e));
   const float wb = (m_b == m) ? 1.0f : (m_b == -INFINITY ? 0.0f : ex2_approx((m_b - m) * kLog2e));
@@ -1590,7 +1605,7 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a) {
   Unit u;
   const int64_t units = (static_cast<int64_t>(a.n_qtiles) + 1) / 2;
   int64_t bh, qu;
-  cta_order(blockIdx.x, units, a.bh, bh, qu);
+  cta_order(blockIdx.x, units, a.bh, a.head_group, bh, qu);
   u.bh = bh;
   u.b = u.bh / a.heads;
   u.h = u.bh % a.heads;
@@ -1903,7 +1918,7 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
     const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
     const float t_nat = mx * a.scale;   // -inf when every key of the tile is masked
     float alpha = 1.0f;
-    const bool resc = t_nat > m_run;
+    const bool resc = t_nat > m_run + kLazyNat;   // the reference moves
     if (resc) {
       alpha = (m_run == -INFINITY) ? 0.0f : ex2_approx((m_run - t_nat) * kLog2e);
       m_run = t_nat;
@@ -1929,7 +1944,7 @@ __device__ __forceinline__ void softmax(const ChunkArgs& a, const Unit& u, int x
     tc_fence_before();
     mbar_arrive(bar(B_PFULL + x));
     const float2 r = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-    l_run = fmaf(l_run, alpha, r.x + r.y);
+    l_run = fmaf(l_run, alpha, (r.x + r.y) + p_max_correction(mx, a.scale_log2, mlog));
   }
   if (!ok) return;
   if (!wait_bar(bar(B_ODONE + x), 0, ctl, budget, R_SOFTMAX, true)) return;

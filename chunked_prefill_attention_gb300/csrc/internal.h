@@ -103,6 +103,8 @@ struct ChunkArgs {
                           // heads that share one K/V plane, row = query row * pack +
                           // head in the group; bh then counts (batch, K/V head) units
                           // and n_qtiles the 128-row tiles of n_q * pack rows; 0 = off
+  int32_t head_group;     // (b, h) units per group in the CTA order (1..8): as many as
+                          // keep the group's K and V of the chunk within 16 MiB of L2
   uint64_t timeout_ns;    // budget of every device-side wait
   // Split form (split_keys > 0): block row y of the grid folds keys
   // [y*split_keys, min((y+1)*split_keys, kv_len)) of the chunk into an empty

@@ -120,6 +120,11 @@ int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
  *   S_ij = scale * Q_i . K_j;   m~_i = max_j S_ij;   m'_i = max(m_i, m~_i);
  *   alpha = e^(m_i - m'_i);     beta_ij = e^(S_ij - m'_i);
  *   l'_i = alpha*l_i + sum_j beta_ij;   O'_i = alpha*O_i + sum_j beta_ij V_j.
+ * The kernels take m' as a reference that moves to the new max only when that
+ * exceeds m by more than 8 ln 2 (otherwise m' = m and alpha = 1): any reference
+ * gives the same O / l, and this one keeps O's rescaling rare.  So after a call
+ * a row that has seen a key holds l = sum e^(S - m) and O = sum e^(S - m) V
+ * over the keys folded so far, with max S - 8 ln 2 <= m <= max S.
  * K and V are the dequantised Q8_0 values d*q.  Only visible keys take part:
  * query row r has position q_pos0 + r, chunk key j has position kv_start + j,
  * and with `causal` the key is visible iff its position <= the query's (the
@@ -144,8 +149,9 @@ int attn_state_init(float *m, float *l, float *o, int64_t batch, int32_t heads,
  * Numerics: Q is fp16; each dequantised key and value d*q is split exactly
  * into an fp16 high part and an fp16 residual, so Q.K and P.V are formed from
  * exact operands on the tensor cores with fp32 accumulation; the weights
- * P = e^(S - m) are rounded to fp16 once, against the running max m (the
- * largest weight of a row is exactly 1); m, l and O stay fp32 in the state.
+ * P = e^(S - m) (at most 2^8) are rounded to fp16 once, and l takes each key
+ * tile's largest weight as rounded (so a row dominated by one key divides by
+ * exactly that key's weight); m, l and O stay fp32 in the state.
  * At D = 128 a CTA folds one 128-row query tile with its two softmax pipelines
  * taking alternate 64-key tiles and merges their states at the end (the same
  * recurrence), so results match D = 64's numerics.

@@ -4,6 +4,8 @@ verification -- 64 candidate queries after the context, rectangular
 full-context attention ("Out-of-Core Flash Streaming & Speculative Decode (1M
 Context)", §4) -- and causal prefill with ragged ranges."""
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -55,10 +57,12 @@ def test_causal_prefill_split(lib, M, chunk, split):
 
 
 def test_split_matches_unsplit(lib):
-    """Split and unsplit forms of the same update: the running max is exact in
-    both, so m is bit-identical; l agrees to fp32 rounding; the weights are
-    rounded to fp16 against each key range's own max before the merge, so the
-    outputs agree within the parity tolerance rather than bit for bit."""
+    """Split and unsplit forms of the same update.  Each keeps its own
+    softmax reference m (the row max, or up to 8 ln 2 below it), so the two
+    m agree within 8 ln 2 and l e^m (the sum of e^S over the keys) agrees to
+    the rounding of the weights; the weights are rounded to fp16 against each
+    key range's own reference before the merge, so the outputs agree within
+    the parity tolerance rather than bit for bit."""
     from chunked_prefill_attention_gb300 import q8attn as Q
     M, H = 2304, 2
     q = seeded((1, 64, H, 64), 41, "cuda", torch.float16)
@@ -69,8 +73,9 @@ def test_split_matches_unsplit(lib):
     Q.attn_chunk_step(q, k8, v8, 0, M, a, q_pos0=M, causal=False)
     Q.attn_chunk_step_split(q, k8, v8, 0, M, b, 256, q_pos0=M, causal=False)
     assert_device_clean()
-    assert torch.equal(a.m, b.m)
-    assert torch.allclose(a.l, b.l, rtol=1e-5, atol=0)
+    lazy = 8 * math.log(2)
+    assert torch.all(torch.abs(a.m - b.m) <= lazy + 1e-4)
+    assert torch.allclose(a.l * torch.exp(a.m - b.m), b.l, rtol=1e-3, atol=0)
     oa, ob = Q.attn_finalize(a).float(), Q.attn_finalize(b).float()
     assert torch.max(torch.abs(oa - ob)).item() <= 2e-3
     want, *_ = oracle_out(q, k, v, causal=False, q_pos0=M)
