@@ -75,6 +75,44 @@ bool q8a::pdl_enabled() { return g_pdl; }
 q8a::PdlScope::PdlScope() : prev(g_pdl) { g_pdl = true; }
 q8a::PdlScope::~PdlScope() { g_pdl = prev; }
 
+// The host-mapped failure word: one page of this library's memory, registered
+// with CUDA on first use (registration pins it; nothing is allocated).  A
+// kernel whose wait runs out stores its status code there as well as in the
+// device word, so q8a_status reads it without a CUDA call.
+namespace {
+alignas(4096) uint32_t g_host_status_page[4096 / sizeof(uint32_t)];
+std::mutex g_host_status_mu;
+std::atomic<int> g_host_status_state{0};   // 0 not tried, 1 registered, 2 registration failed
+uint32_t* g_host_status_dev = nullptr;
+}  // namespace
+
+uint32_t* q8a::host_status_word() {
+  const int st = g_host_status_state.load(std::memory_order_acquire);
+  if (st != 0) return st == 1 ? g_host_status_dev : nullptr;
+  std::lock_guard<std::mutex> lock(g_host_status_mu);
+  if (g_host_status_state.load(std::memory_order_relaxed) == 0) {
+    // registration is not a stream operation; relaxed capture mode keeps it
+    // legal while this or another thread is capturing a stream
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    int result = 2;
+    if (cudaHostRegister(g_host_status_page, sizeof(g_host_status_page),
+                         cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+      void* dev = nullptr;
+      if (cudaHostGetDevicePointer(&dev, g_host_status_page, 0) == cudaSuccess) {
+        g_host_status_dev = static_cast<uint32_t*>(dev);
+        result = 1;
+      } else {
+        cudaHostUnregister(g_host_status_page);
+      }
+    }
+    if (result != 1) cudaGetLastError();   // the failure is reported by q8a_status, not later calls
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    g_host_status_state.store(result, std::memory_order_release);
+  }
+  return g_host_status_state.load(std::memory_order_relaxed) == 1 ? g_host_status_dev : nullptr;
+}
+
 const char* q8a::launch_note() { return g_note; }
 
 void q8a::set_launch_note(const char* fmt, ...) {
@@ -245,6 +283,7 @@ int prepare_chunk_step(const char* fn, const void* q, int64_t q_pos0, const void
     a->head_group = static_cast<int32_t>(g < 1 ? 1 : (g > 8 ? 8 : g));
   }
   a->timeout_ns = g_timeout_ns.load();
+  a->host_status = q8a::host_status_word();
   return Q8A_OK;
 }
 
@@ -575,11 +614,27 @@ int attn_finalize(const float* l, const float* o, void* out, int64_t batch, int3
 int q8a_device_status(void* stream, uint32_t* status_out, int32_t clear) {
   uint32_t s = 0;
   cudaError_t e = q8a::read_device_status(static_cast<cudaStream_t>(stream), &s, clear != 0);
+  if (e == cudaSuccess && clear) __atomic_store_n(&g_host_status_page[0], 0u, __ATOMIC_RELEASE);
   if (status_out) *status_out = s;
   if (e != cudaSuccess) return cuda_fail(e, "q8a_device_status");
   if (s != 0)
     return fail(Q8A_ERR_TIMEOUT, "q8a_device_status: a device-side wait ran out (status 0x%x, role %u)",
                 s, (s >> 8) & 0xFFu);
+  return ok();
+}
+
+int q8a_status(void* stream) {
+  if (g_host_status_state.load(std::memory_order_acquire) == 2)
+    return fail(Q8A_ERR_UNSUPPORTED, "q8a_status: the host-mapped status word could not be registered; "
+                                     "use q8a_device_status");
+  if (stream) {
+    const cudaError_t e = cudaStreamQuery(static_cast<cudaStream_t>(stream));   // does not block
+    if (e != cudaSuccess && e != cudaErrorNotReady) return cuda_fail(e, "q8a_status");
+  }
+  const uint32_t s = __atomic_load_n(&g_host_status_page[0], __ATOMIC_ACQUIRE);
+  if (s != 0)
+    return fail(Q8A_ERR_TIMEOUT, "q8a_status: a device-side wait ran out (status 0x%x, role %u)", s,
+                (s >> 8) & 0xFFu);
   return ok();
 }
 

@@ -152,6 +152,16 @@ __device__ __forceinline__ bool budget_ran_out(Ctl* ctl, long long t0, uint64_t 
   return false;
 }
 
+// A CTA whose wait ran out copies the status word (the first failure of the
+// device) into the host-mapped word, which q8a_status reads without any
+// synchronisation.  Called once per CTA after its roles have stopped, so the
+// waits themselves only set the abort flag and the device word.
+__device__ __forceinline__ void publish_failure(uint32_t* host_word) {
+  const uint32_t code = *reinterpret_cast<volatile uint32_t*>(&g_status);
+  *reinterpret_cast<volatile uint32_t*>(host_word) = code ? code : 1u;
+  __threadfence_system();
+}
+
 // Warp-uniform bounded wait on an mbarrier phase.  All 32 lanes call it
 // together.  Returns false when the CTA is aborting (honour_abort) or the
 // budget ran out; in the latter case the first failure is recorded.  The budget
@@ -947,6 +957,8 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && a.host_status && *reinterpret_cast<volatile uint32_t*>(&ctl->abort))
+    publish_failure(a.host_status);
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -1520,6 +1532,8 @@ chunk_step_d128_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && a.host_status && *reinterpret_cast<volatile uint32_t*>(&ctl->abort))
+    publish_failure(a.host_status);
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -2016,6 +2030,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_step_d128x2_kernel(const Ch
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && a.host_status && *reinterpret_cast<volatile uint32_t*>(&ctl->abort))
+    publish_failure(a.host_status);
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);

@@ -106,6 +106,7 @@ struct ChunkArgs {
   int32_t head_group;     // (b, h) units per group in the CTA order (1..8): as many as
                           // keep the group's K and V of the chunk within 16 MiB of L2
   uint64_t timeout_ns;    // budget of every device-side wait
+  uint32_t* host_status;  // device address of the host-mapped failure word, or null
   // Split form (split_keys > 0): block row y of the grid folds keys
   // [y*split_keys, min((y+1)*split_keys, kv_len)) of the chunk into an empty
   // partial state at part_m/part_l/part_o + y * (bh*n_q) rows; the partials
@@ -132,6 +133,11 @@ int chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const void
                      float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
                      float scale, int32_t causal, int64_t tile_begin, int64_t tile_end,
                      cudaStream_t stream);
+
+// Device address of the host-mapped failure word that q8a_status reads (the
+// first call registers the library's page for it), or null when the page could
+// not be registered.
+uint32_t* host_status_word();
 
 // Record `msg` as the calling thread's last error (q8a_last_error) and return code.
 int set_error(int code, const char* fn, const char* msg);

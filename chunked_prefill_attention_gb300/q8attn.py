@@ -60,6 +60,7 @@ SIGNATURES = {
     "q8a_prefill_graph_launch": (ctypes.c_int, [_P, _P]),
     "q8a_prefill_graph_destroy": (ctypes.c_int, [_P]),
     "q8a_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _I32]),
+    "q8a_status": (ctypes.c_int, [_P]),
     "q8a_set_wait_timeout_ns": (ctypes.c_int, [_U64]),
     "q8a_test_inject": (ctypes.c_int, [_I32]),
 }
@@ -375,6 +376,13 @@ def device_status(clear=True, stream=None):
     s = ctypes.c_void_p(stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream)
     rc = load().q8a_device_status(s, ctypes.byref(st), 1 if clear else 0)
     return rc, st.value
+
+
+def status(stream=None):
+    """Return code of the sync-free status check (q8a_status): Q8A_OK, or
+    Q8A_ERR_TIMEOUT once a kernel has recorded a run-out wait."""
+    s = ctypes.c_void_p(stream.cuda_stream if stream is not None else None)
+    return load().q8a_status(s)
 
 
 def set_wait_timeout_ns(ns):

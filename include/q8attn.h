@@ -59,8 +59,8 @@ extern "C" {
  * head_dim 128 and q8a_plane_stride_bytes_for.  5: the captured prefill
  * (q8a_prefill_graph_*).  6: attn_prefill_pipelined and the split calls at
  * head_dim 128, q8a_prefill_slot_floats_for, q8a_split_workspace_floats_for and
- * attn_chunk_step_split_gqa. */
-#define Q8A_ABI_VERSION 6u
+ * attn_chunk_step_split_gqa.  7: q8a_status. */
+#define Q8A_ABI_VERSION 7u
 
 enum {
   Q8A_OK = 0,
@@ -400,6 +400,25 @@ int q8a_prefill_graph_destroy(q8a_prefill_graph *graph);
  * or Q8A_ERR_CUDA.  status_out may be NULL.
  */
 int q8a_device_status(void *stream, uint32_t *status_out, int32_t clear);
+
+/*
+ * q8a_status -- the sync-free status check: whether any kernel of this library
+ * has recorded a device-side wait that ran out since the last clear, read from
+ * a host-mapped word without synchronising anything and without blocking.  A
+ * kernel that gives up stores its status code (as q8a_device_status reports
+ * it) into that word as well as into the device word; the store reaches the
+ * host as the kernel runs, so the answer covers the library's kernels that have
+ * run so far on any stream, not work still queued.  The word is one page of the
+ * library's own memory, registered with CUDA (cudaHostRegister, mapped and
+ * portable) by the first chunk-step call of the process; nothing is allocated.
+ * q8a_device_status with `clear` clears it too.
+ *   stream   if not NULL, also asks cudaStreamQuery(stream), which does not
+ *            block, and reports a CUDA error that the stream's work raised.
+ * Returns Q8A_OK, Q8A_ERR_TIMEOUT (a wait ran out; q8a_last_error() names the
+ * role), Q8A_ERR_CUDA (from cudaStreamQuery) or Q8A_ERR_UNSUPPORTED (the page
+ * could not be registered: use q8a_device_status).
+ */
+int q8a_status(void *stream);
 
 /* Budget of every device-side wait, in nanoseconds (default 2e9; minimum 1e6).
  * Applies to launches made after the call, from any thread. */

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), f"missing export {n}"
         assert n in q8attn.SIGNATURES, f"binding lacks {n}"
-    assert lib.q8a_abi_version() == 6
+    assert lib.q8a_abi_version() == 7
 
 
 def test_plane_stride(lib):
@@ -255,3 +255,9 @@ def test_head_dim_128_strides_and_split_sizes(lib):
     rc = lib.attn_chunk_step_split_static(A16, 0, A16, A16, 136 * 512, 0, 512, A16, A16, A16, 1, 2, 64,
                                           96, 0.125, 0, 128, s)
     assert rc == Q.Q8A_ERR_UNSUPPORTED
+
+def test_status_before_any_launch_is_ok(lib):
+    """The sync-free check makes no CUDA call without a stream: before any
+    chunk step has run (nothing registered, nothing failed) it answers OK."""
+    from chunked_prefill_attention_gb300 import q8attn as Q
+    assert lib.q8a_status(None) == Q.Q8A_OK

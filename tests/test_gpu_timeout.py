@@ -22,13 +22,18 @@ def test_wait_budget_runs_out_cleanly(lib):
     st = Q.State(1, 1, 128, "cuda")
     rc, _ = Q.device_status(clear=True)
     assert rc == Q.Q8A_OK
+    assert Q.status() == Q.Q8A_OK
     Q.set_wait_timeout_ns(50_000_000)
     try:
         Q.test_inject(1)
         Q.attn_chunk_step(q, k8, v8, 0, 128, st)
+        torch.cuda.current_stream().synchronize()
+        # the sync-free check sees the failure through the host-mapped word
+        assert Q.status(torch.cuda.current_stream()) == Q.Q8A_ERR_TIMEOUT
         rc, status = Q.device_status(clear=True)
         assert rc == Q.Q8A_ERR_TIMEOUT
         assert status & 1 and ((status >> 8) & 0xFF) in (1, 2, 3, 4, 5)
+        assert Q.status() == Q.Q8A_OK   # cleared with the device word
     finally:
         Q.test_inject(0)
         Q.set_wait_timeout_ns(2_000_000_000)
@@ -36,5 +41,6 @@ def test_wait_budget_runs_out_cleanly(lib):
     out, *_ = run_gpu(q, k, v, 128)
     rc, status = Q.device_status(clear=True)
     assert rc == Q.Q8A_OK and status == 0
+    assert Q.status() == Q.Q8A_OK
     want, *_ = oracle_out(q, k, v)
     compare(out.cpu().numpy(), want, "after timeout")
