@@ -405,10 +405,10 @@ int q8a_device_status(void *stream, uint32_t *status_out, int32_t clear);
  * q8a_status -- the sync-free status check: whether any kernel of this library
  * has recorded a device-side wait that ran out since the last clear, read from
  * a host-mapped word without synchronising anything and without blocking.  A
- * kernel that gives up stores its status code (as q8a_device_status reports
- * it) into that word as well as into the device word; the store reaches the
- * host as the kernel runs, so the answer covers the library's kernels that have
- * run so far on any stream, not work still queued.  The word is one page of the
+ * block of a kernel whose wait ran out copies the device's status code (as
+ * q8a_device_status reports it) into that word once its roles have stopped;
+ * the store reaches the host while the kernel runs, so the answer covers the
+ * library's kernels that have run so far on any stream, not work still queued.  The word is one page of the
  * library's own memory, registered with CUDA (cudaHostRegister, mapped and
  * portable) by the first chunk-step call of the process; nothing is allocated.
  * q8a_device_status with `clear` clears it too.
