@@ -120,6 +120,9 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
   // block as the rows arrive, so only chunk 0's K and V and the first block of
   // Q cross the link before the device starts.
   const int64_t q_block = ((chunk < 8192 ? chunk : 8192) + 255) / 256 * 256;
+  // leads of chunk 0 (causal): a multiple of 256 rows (two query tiles) whose
+  // Q8_0 rows start 16-byte aligned at either head_dim
+  constexpr int64_t kLead = 1024;
   const size_t q_row_bytes = static_cast<size_t>(row_floats) * 2;   // one token, all heads, fp16
 
   // With the causal mask (q_pos0 = 0) no later chunk touches the query rows of
@@ -134,6 +137,70 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
     float* ks = kv_slots + 2 * slot * part;
     float* vs = ks + part;
     const size_t bytes = static_cast<size_t>(n * row_floats) * sizeof(float);
+    const uint8_t* kc = static_cast<const uint8_t*>(k8) + s0 * q8_row;
+    const uint8_t* vc = static_cast<const uint8_t*>(v8) + s0 * q8_row;
+    if (c == 0 && causal && (n % kLead == 0 || n == n_tokens)) {
+      // Chunk 0 with the mask: its K, V and query rows cross in leads of kLead
+      // tokens, and as each lead arrives it is quantised and its rows are
+      // folded with chunk 0's keys up to them (the later keys of the chunk are
+      // masked for them), so the device starts after one lead instead of the
+      // whole chunk.  The same key tiles in the same order as one chunk-0 step.
+      for (int64_t j0 = 0; j0 < n; j0 += kLead) {
+        const int64_t nj = (n - j0 < kLead) ? n - j0 : kLead;
+        const size_t kv_bytes = static_cast<size_t>(nj * row_floats) * sizeof(float);
+        for (int64_t b = 0; b < batch; ++b) {
+          const int64_t src = (b * n_tokens + j0) * row_floats;
+          const int64_t dst = (b * slot_tokens + j0) * row_floats;
+          const size_t qoff = static_cast<size_t>(b * n_tokens + j0) * q_row_bytes;
+          if ((e = cudaMemcpyAsync(ks + dst, k_host + src, kv_bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
+              (e = cudaMemcpyAsync(vs + dst, v_host + src, kv_bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
+              (e = cudaMemcpyAsync(static_cast<uint8_t*>(q_dev) + qoff, static_cast<const uint8_t*>(q_host) + qoff,
+                                   static_cast<size_t>(nj) * q_row_bytes, cudaMemcpyHostToDevice, xs)) !=
+                  cudaSuccess)
+            return bail(cuda_err(e, "copy of a lead of chunk 0"));
+        }
+        if ((e = cudaEventRecord(ev, xs)) != cudaSuccess || (e = cudaStreamWaitEvent(cs, ev, 0)) != cudaSuccess)
+          return bail(cuda_err(e, "cudaEventRecord / cudaStreamWaitEvent"));
+        for (int64_t b = 0; b < batch; ++b) {
+          const int64_t off = (b * slot_tokens + j0) * row_floats;
+          uint8_t* kq = static_cast<uint8_t*>(k8) + b * heads * plane_stride_bytes + j0 * q8_row;
+          uint8_t* vq = static_cast<uint8_t*>(v8) + b * heads * plane_stride_bytes + j0 * q8_row;
+          if ((rc = q8kv_quantize(ks + off, kq, 1, nj, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK ||
+              (rc = q8kv_quantize(vs + off, vq, 1, nj, heads, head_dim, plane_stride_bytes, cs)) != Q8A_OK)
+            return bail(rc);
+        }
+        if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, 0, j0 + nj, m, l, o, batch, heads,
+                                        n_tokens, head_dim, scale, causal, j0 / 128, (j0 + nj + 127) / 128,
+                                        cs)) != Q8A_OK)
+          return bail(rc);
+      }
+      if ((e = cudaEventRecord(ev_free[slot], cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+      // the rows after chunk 0 in blocks, each folded with the whole chunk as it arrives
+      for (int64_t r0 = n; r0 < n_tokens; r0 += q_block) {
+        const int64_t nr = (n_tokens - r0 < q_block) ? n_tokens - r0 : q_block;
+        for (int64_t b = 0; b < batch; ++b) {
+          const size_t off = static_cast<size_t>(b * n_tokens + r0) * q_row_bytes;
+          if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(q_dev) + off, static_cast<const uint8_t*>(q_host) + off,
+                                   static_cast<size_t>(nr) * q_row_bytes, cudaMemcpyHostToDevice, xs)) !=
+              cudaSuccess)
+            return bail(cuda_err(e, "copy of a block of Q"));
+        }
+        if ((e = cudaEventRecord(ev_q, xs)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(cs, ev_q, 0)) != cudaSuccess)
+          return bail(cuda_err(e, "cudaEventRecord / cudaStreamWaitEvent"));
+        if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
+                                        n_tokens, head_dim, scale, causal, r0 / 128, (r0 + nr + 127) / 128,
+                                        cs)) != Q8A_OK)
+          return bail(rc);
+      }
+      if ((e = q8a::launch_finalize_rows(l, o, out_dev, batch, heads, n_tokens, head_dim, s0, n, cs)) !=
+          cudaSuccess)
+        return bail(cuda_err(e, "finalize of a row block"));
+      if ((e = cudaEventRecord(ev_fin, cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
+      prev_r0 = s0;
+      prev_n = n;
+      continue;
+    }
     // the slot's previous chunk (c - 2) must have been quantised before it is refilled
     if (c >= 2 && (e = cudaStreamWaitEvent(xs, ev_free[slot], 0)) != cudaSuccess)
       return bail(cuda_err(e, "cudaStreamWaitEvent"));
@@ -162,8 +229,6 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
         return bail(rc);
     }
     if ((e = cudaEventRecord(ev_free[slot], cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
-    const uint8_t* kc = static_cast<const uint8_t*>(k8) + s0 * q8_row;
-    const uint8_t* vc = static_cast<const uint8_t*>(v8) + s0 * q8_row;
     if (c == 0) {
       for (int64_t r0 = 0; r0 < n_tokens; r0 += q_block) {
         const int64_t nr = (n_tokens - r0 < q_block) ? n_tokens - r0 : q_block;

@@ -297,7 +297,11 @@ int attn_finalize(const float *l, const float *o, void *out, int64_t batch, int3
  * the slot into the Q8_0 planes, attn_chunk_step with kv_start = the chunk's
  * first token, q_pos0 = 0); a slot is refilled only after the quantise that
  * read it.  Q crosses after chunk 0's K and V, in blocks of up to 8,192 rows,
- * and chunk 0's step runs block by block as they arrive.  The fp32 inputs so take 2 x 2 x B x chunk x H x 64 floats of device
+ * and chunk 0's step runs block by block as they arrive; with `causal` and a
+ * chunk 0 of a multiple of 1,024 tokens (or the whole sequence), chunk 0's K,
+ * V and query rows cross together in leads of 1,024 tokens, each quantised and
+ * folded (its rows against chunk 0's keys up to them) as it arrives.  The fp32
+ * inputs so take 2 x 2 x B x chunk x H x 64 floats of device
  * memory whatever the sequence length.  With `causal` no later chunk touches a
  * chunk's own query rows, so those rows are finalised right after its step and
  * copied back to the host on copy_stream while the device works on the later

@@ -13,13 +13,17 @@ pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="
 
 
 @pytest.mark.parametrize("B,M,H,chunk", [(1, 1000, 2, 256), (2, 768, 3, 128), (1, 2048, 4, 2048),
-                                         (2, 2600, 3, 256), (1, 17000, 2, 8192)])
+                                         (2, 2600, 3, 256), (1, 17000, 2, 8192), (2, 5000, 3, 2048),
+                                         (1, 1500, 2, 2048)])
 def test_pipelined_matches_device_path(lib, B, M, H, chunk):
     """The K/V slots hold two chunks: with M > 2 * chunk each slot is refilled
     several times (one case streams 11 chunks through them).  Q follows chunk
     0's K and V in row blocks, and chunk 0's step runs per block (blocks of
-    256 rows for the small chunks, 8,192 for the last case, with a ragged
-    last block)."""
+    256 rows for the small chunks, 8,192 for the 17,000-token case, with a
+    ragged last block).  When chunk 0 is a multiple of 1,024 tokens (or the
+    whole sequence) its K, V and query rows cross in leads of 1,024 tokens,
+    each folded as it arrives (two batch entries with later row blocks; a
+    single 1,500-token chunk whose last lead holds a partial query tile)."""
     from chunked_prefill_attention_gb300 import q8attn as Q
     q = seeded((B, M, H, 64), M + 71, "cuda", torch.float16)
     k = seeded((B, M, H, 64), M + 72, "cuda")
