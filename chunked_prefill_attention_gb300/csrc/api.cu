@@ -319,7 +319,7 @@ int q8a::chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const
                           int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
                           float* l, float* o, int64_t batch, int32_t heads, int64_t n_q,
                           int32_t head_dim, float scale, int32_t causal, int64_t tile_begin,
-                          int64_t tile_end, cudaStream_t stream) {
+                          int64_t tile_end, bool l2_keep_kv, cudaStream_t stream) {
   const char* fn = "attn_chunk_step";
   CUtensorMap qmap;
   q8a::ChunkArgs a;
@@ -339,6 +339,7 @@ int q8a::chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const
     return fail(Q8A_ERR_INVALID_ARG, "%s: an interior range of an odd number of query tiles", fn);
   a.tile0 = static_cast<int32_t>(t0);
   a.n_qtiles = static_cast<int32_t>(t1 - t0);
+  a.l2_keep_kv = (l2_keep_kv && head_dim == 64 && aligned(o, 32)) ? 1 : 0;
   cudaError_t e = head_dim == 128 ? q8a::launch_chunk_step_d128(qmap, a, stream)
                                   : q8a::launch_chunk_step(qmap, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, fn);

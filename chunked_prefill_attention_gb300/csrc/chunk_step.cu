@@ -363,6 +363,9 @@ __device__ __forceinline__ Unit make_unit(const ChunkArgs& a, const Range& kr) {
 
 // ------------------------------------------------------------------ roles --
 
+// kKeep: the pipelined prefill's form (ChunkArgs::l2_keep_kv), a separate
+// instantiation so that the other launches run exactly the plain code.
+template <bool kKeep>
 __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const ChunkArgs& a,
                                               const Range& kr, const Unit& u, uint8_t* smem,
                                               uint32_t sbase, Ctl* ctl) {
@@ -384,6 +387,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* qmap, const Chu
             tma_load_3d(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL), 0,
                         static_cast<int32_t>(u.h * a.pack),
                         static_cast<int32_t>(u.b * a.n_q + (u.r0 + tile_row0(a, x)) / a.pack));
+          else if (kKeep)   // Q is read once: evict-first, the chunk's K/V stay in L2
+            tma_load_3d_hint(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL),
+                             static_cast<int32_t>(u.h * kHeadDim), static_cast<int32_t>(u.r0 + tile_row0(a, x)),
+                             static_cast<int32_t>(u.b), l2_evict_first_policy());
           else
             tma_load_3d(sbase + OFF_Q + x * 16384, qmap, bar(B_QFULL),
                         static_cast<int32_t>(u.h * kHeadDim), static_cast<int32_t>(u.r0 + tile_row0(a, x)),
@@ -696,6 +703,7 @@ __device__ __forceinline__ void merge_pair_out(const Range& kr, int64_t sidx, bo
   }
 }
 
+template <bool kKeep>
 __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr, const Unit& u, int x,
                                              uint8_t* smem, uint32_t sbase, uint32_t tmem, Ctl* ctl) {
   const uint64_t budget = 2 * a.timeout_ns;   // cycles
@@ -721,13 +729,29 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
   const bool pair_merge = a.pair && u.T[1] > 0;
   float m_run = -INFINITY, l_run = 0.0f;
   if (active && !fresh) {
-    m_run = kr.m[sidx];
-    l_run = kr.l[sidx];
+    if (kKeep) {   // the state is read once: evict-first, the chunk's K/V stay in L2
+      const uint64_t pol = l2_evict_first_policy();
+      m_run = ld_hint(kr.m + sidx, pol);
+      l_run = ld_hint(kr.l + sidx, pol);
+    } else {
+      m_run = kr.m[sidx];
+      l_run = kr.l[sidx];
+    }
   }
   {
     // the O row enters TMEM as the high half; the residual half starts at 0
     uint32_t oh[64];
-    if (active && !fresh) {
+    if (kKeep && active && !fresh) {
+      const uint64_t pol = l2_evict_first_policy();
+      const float* src = kr.o + sidx * kHeadDim;   // 32-byte aligned (checked on the host)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t w[8];
+        ld8_hint(src + 8 * i, w, pol);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) oh[8 * i + e] = w[e];
+      }
+    } else if (active && !fresh) {
       const float4* src = reinterpret_cast<const float4*>(kr.o + sidx * kHeadDim);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -874,7 +898,11 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
         merge_pair_out(kr, sidx, active, m_run, l_run, pb.x, pb.y, t_o, t_o + 128u);
         return;
       }
-      if (active) {
+      if (kKeep && active) {
+        const uint64_t pol = l2_evict_first_policy();
+        st_hint(kr.m + sidx, m_run, pol);
+        st_hint(kr.l + sidx, l_run, pol);
+      } else if (active) {
         kr.m[sidx] = m_run;
         kr.l[sidx] = l_run;
       }
@@ -885,7 +913,17 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
         tmem_ld32(t_o + 64 + 32 * half, ol);
         tmem_wait_ld(oh);
         tmem_wait_ld(ol);
-        if (active) {
+        if (kKeep && active) {
+          const uint64_t pol = l2_evict_first_policy();
+          float* dst = kr.o + sidx * kHeadDim + 32 * half;   // whole 32-byte sectors
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(oh[8 * i + e]) + __uint_as_float(ol[8 * i + e]);
+            st8_hint(dst + 8 * i, v, pol);
+          }
+        } else if (active) {
           float4* dst = reinterpret_cast<float4*>(kr.o + sidx * kHeadDim) + 8 * half;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -901,6 +939,7 @@ __device__ __forceinline__ void softmax_role(const ChunkArgs& a, const Range& kr
   }
 }
 
+template <bool kKeep>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -943,13 +982,13 @@ chunk_step_kernel(const __grid_constant__ CUtensorMap qmap, const ChunkArgs a) {
   // fragments; the other warpgroups need far fewer registers.
   if (wg < 2) {
     reg_alloc<kRegSoftmax>();
-    softmax_role(a, kr, u, wg, smem, sbase, tmem, ctl);
+    softmax_role<kKeep>(a, kr, u, wg, smem, sbase, tmem, ctl);
   } else {
     reg_dealloc<kRegOther>();
     if (wg == 2) {
       dequant_role(a, kr, u, smem, sbase, ctl);
     } else if (warp == 12) {
-      producer_role(&qmap, a, kr, u, smem, sbase, ctl);
+      producer_role<kKeep>(&qmap, a, kr, u, smem, sbase, ctl);
     } else if (warp == 13) {
       mma_role(a, u, sbase, tmem, ctl);
     }
@@ -2048,20 +2087,21 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(chunk_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-    if (e != cudaSuccess) return e;
     // The setmaxnreg split assumes every thread is launched with 65536 / 512
     // registers; with fewer, an increase could wait forever, so such a build is
     // refused before any launch.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, chunk_step_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs * kThreads != 65536 || fa.maxThreadsPerBlock < kThreads) {
-      set_launch_note("chunk_step_kernel has %d registers per thread and at most %d threads per "
-                      "block; the register split needs %d and %d",
-                      fa.numRegs, fa.maxThreadsPerBlock, 65536 / kThreads, kThreads);
-      return cudaErrorInvalidConfiguration;
+    for (auto* fn : {chunk_step_kernel<false>, chunk_step_kernel<true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs * kThreads != 65536 || fa.maxThreadsPerBlock < kThreads) {
+        set_launch_note("chunk_step_kernel has %d registers per thread and at most %d threads per "
+                        "block; the register split needs %d and %d",
+                        fa.numRegs, fa.maxThreadsPerBlock, 65536 / kThreads, kThreads);
+        return cudaErrorInvalidConfiguration;
+      }
     }
     configured_device = dev;
   }
@@ -2072,8 +2112,8 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const unsigned gy = args.split_keys > 0 ? static_cast<unsigned>(args.n_splits) : 1u;
-  e = launch_kernel(chunk_step_kernel, dim3(static_cast<unsigned>(blocks), gy), dim3(kThreads), SMEM_BYTES, stream,
-                    qmap, units);
+  e = launch_kernel(args.l2_keep_kv ? chunk_step_kernel<true> : chunk_step_kernel<false>,
+                    dim3(static_cast<unsigned>(blocks), gy), dim3(kThreads), SMEM_BYTES, stream, qmap, units);
   if (e != cudaSuccess)
     set_launch_note("chunk_step_kernel<<<(%lld, %u), %d, %d>>>", static_cast<long long>(blocks), gy,
                     kThreads, SMEM_BYTES);

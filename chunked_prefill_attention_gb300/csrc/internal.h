@@ -105,6 +105,10 @@ struct ChunkArgs {
                           // and n_qtiles the 128-row tiles of n_q * pack rows; 0 = off
   int32_t head_group;     // (b, h) units per group in the CTA order (1..8): as many as
                           // keep the group's K and V of the chunk within 16 MiB of L2
+  int32_t l2_keep_kv;     // 1: Q and the running state go through L2 with the evict-first
+                          // policy (whole 32-byte sectors), so that the chunk's Q8_0 rows,
+                          // quantised just before the step, stay in L2 for every CTA
+                          // that reads them (the pipelined prefill; head_dim 64)
   uint64_t timeout_ns;    // budget of every device-side wait
   uint32_t* host_status;  // device address of the host-mapped failure word, or null
   // Split form (split_keys > 0): block row y of the grid folds keys
@@ -127,12 +131,14 @@ cudaError_t launch_chunk_step(const CUtensorMap& qmap, const ChunkArgs& args, cu
 // no split form.
 cudaError_t launch_chunk_step_d128(const CUtensorMap& qmap, const ChunkArgs& args, cudaStream_t stream);
 
-// attn_chunk_step for the 128-row query tiles [tile_begin, tile_end) only.
+// attn_chunk_step for the 128-row query tiles [tile_begin, tile_end) only;
+// l2_keep_kv sets ChunkArgs::l2_keep_kv (the chunk was quantised just before,
+// and o is 32-byte aligned).
 int chunk_step_tiles(const void* q, int64_t q_pos0, const void* k_q8, const void* v_q8,
                      int64_t kv_plane_stride_bytes, int64_t kv_start, int64_t kv_len, float* m,
                      float* l, float* o, int64_t batch, int32_t heads, int64_t n_q, int32_t head_dim,
                      float scale, int32_t causal, int64_t tile_begin, int64_t tile_end,
-                     cudaStream_t stream);
+                     bool l2_keep_kv, cudaStream_t stream);
 
 // Device address of the host-mapped failure word that q8a_status reads (the
 // first call registers the library's page for it), or null when the page could

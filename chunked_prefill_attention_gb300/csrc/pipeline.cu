@@ -171,7 +171,7 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
         }
         if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, 0, j0 + nj, m, l, o, batch, heads,
                                         n_tokens, head_dim, scale, causal, j0 / 128, (j0 + nj + 127) / 128,
-                                        cs)) != Q8A_OK)
+                                        true, cs)) != Q8A_OK)
           return bail(rc);
       }
       if ((e = cudaEventRecord(ev_free[slot], cs)) != cudaSuccess) return bail(cuda_err(e, "cudaEventRecord"));
@@ -190,7 +190,7 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
           return bail(cuda_err(e, "cudaEventRecord / cudaStreamWaitEvent"));
         if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
                                         n_tokens, head_dim, scale, causal, r0 / 128, (r0 + nr + 127) / 128,
-                                        cs)) != Q8A_OK)
+                                        true, cs)) != Q8A_OK)
           return bail(rc);
       }
       if ((e = q8a::launch_finalize_rows(l, o, out_dev, batch, heads, n_tokens, head_dim, s0, n, cs)) !=
@@ -245,11 +245,12 @@ int attn_prefill_pipelined(const void* q_host, const float* k_host, const float*
           return bail(cuda_err(e, "cudaEventRecord / cudaStreamWaitEvent"));
         if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
                                         n_tokens, head_dim, scale, causal, r0 / 128, (r0 + nr + 127) / 128,
-                                        cs)) != Q8A_OK)
+                                        true, cs)) != Q8A_OK)
           return bail(rc);
       }
-    } else if ((rc = attn_chunk_step(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
-                                     n_tokens, head_dim, scale, causal, cs)) != Q8A_OK) {
+    } else if ((rc = q8a::chunk_step_tiles(q_dev, 0, kc, vc, plane_stride_bytes, s0, n, m, l, o, batch, heads,
+                                           n_tokens, head_dim, scale, causal, 0, (n_tokens + 127) / 128, true,
+                                           cs)) != Q8A_OK) {
       return bail(rc);
     }
     if (causal) {

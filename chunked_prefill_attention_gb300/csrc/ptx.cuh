@@ -97,13 +97,45 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 // --------------------------------------------------- L2 eviction priority --
 // A cache policy that marks the lines it touches as the first to leave L2.
-// Given to the loads of data a kernel reads once (the quantiser's fp32 input),
-// so that they do not push out lines that are read again soon: the Q8_0 rows
-// a quantise has just written for the chunk step that follows it.
+// Given to the loads of data a kernel reads once (the quantiser's fp32 input;
+// in the pipelined prefill, the chunk step's Q tiles and running state), so
+// that they do not push out lines that are read again soon: the Q8_0 rows a
+// quantise has just written for the chunk step that follows it.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// tma_load_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t c0, int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+// 32-byte (one sector) global load / store of eight floats with an L2 cache
+// policy; p is 32-byte aligned.  A whole sector per access, so an evict-first
+// line is never wanted again after it is evicted.
+__device__ __forceinline__ void ld8_hint(const float* p, uint32_t (&v)[8], uint64_t policy) {
+  asm volatile("ld.global.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p), "l"(policy));
+}
+__device__ __forceinline__ void st8_hint(float* p, const float (&v)[8], uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
+               "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ float ld_hint(const float* p, uint64_t policy) {
+  float v;
+  asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
