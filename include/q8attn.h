@@ -14,9 +14,11 @@
  *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates, frees or synchronises on its own; every compute call is
- *     one or more asynchronous kernel launches on `stream` (a cudaStream_t
- *     passed as void*; NULL is the legacy default stream).
+ *     never allocates, frees or synchronises on its own (q8a_device_status, which
+ *     says so, synchronises its stream; the first chunk-step call of the process
+ *     pins one page of the library's own memory for q8a_status); every compute
+ *     call is one or more asynchronous kernel launches on `stream` (a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream).
  *   - Return value: Q8A_OK (0) or a negative Q8A_ERR_* code.  Arguments are
  *     validated on the host before any CUDA call, so argument errors are
  *     reported without touching the device.  q8a_last_error() returns a
